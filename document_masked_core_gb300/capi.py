@@ -1,0 +1,254 @@
+"""ctypes binding of libca.so (include/ca.h), argument marshalling only.
+
+Every computation runs in the library's CUDA kernels.  If libca.so is missing
+or cannot be loaded, every entry point raises: there is no fallback.  Torch
+tensors are accepted for device buffers (their data pointers are passed);
+torch is used here only for memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libca.so")
+
+CA_OK = 0
+CA_ERR_INVALID_ARG = 1
+CA_ERR_UNSUPPORTED = 2
+CA_ERR_CUDA = 3
+CA_ERR_DEVICE_TIMEOUT = 4
+CA_ERR_DEVICE_BOUNDS = 5
+CA_ERR_NO_DEVICE = 6
+CA_DTYPE_BF16 = 0
+CA_DTYPE_FP32 = 1
+
+# names declared in include/ca.h, in order
+EXPORTS = [
+    "ca_plan_create", "ca_plan_dry_run", "ca_plan_info", "ca_plan_task_pairs", "ca_plan_destroy",
+    "ca_forward", "ca_backward", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
+    "ca_watchdog_selftest", "ca_status_string", "ca_last_error", "ca_version",
+]
+
+
+class CAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"[{status}] {msg}")
+        self.status = status
+
+
+class Task(ctypes.Structure):
+    _fields_ = [("doc_id", ctypes.c_int32), ("reserved", ctypes.c_int32), ("q_start", ctypes.c_int64),
+                ("q_len", ctypes.c_int64), ("kv_start", ctypes.c_int64), ("kv_len", ctypes.c_int64)]
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("o_dtype", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "total_q", "total_kv", "n_tasks", "n_docs", "causal_pairs", "flops_fwd", "flops_bwd",
+        "workspace_bytes", "n_fwd_items", "n_bwd_items", "fwd_tile_pairs", "bwd_tile_pairs")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libca.so (raises if it is missing: build it with
+    ``document_masked_core_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libca.so not found at {p}; run document_masked_core_gb300.build.build() first")
+    L = ctypes.CDLL(p)
+    vp, i32, i64, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    L.ca_plan_create.restype = st
+    L.ca_plan_create.argtypes = [ctypes.POINTER(Task), i32, vp, vp, i32, ctypes.POINTER(Shape), vp,
+                                 ctypes.POINTER(vp)]
+    L.ca_plan_dry_run.restype = st
+    L.ca_plan_dry_run.argtypes = [ctypes.POINTER(Task), i32, vp, vp, i32, ctypes.POINTER(Shape),
+                                  ctypes.POINTER(PlanInfo), vp]
+    L.ca_plan_info.restype = st
+    L.ca_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    L.ca_plan_task_pairs.restype = st
+    L.ca_plan_task_pairs.argtypes = [vp, vp]
+    L.ca_plan_destroy.restype = None
+    L.ca_plan_destroy.argtypes = [vp]
+    L.ca_forward.restype = st
+    L.ca_forward.argtypes = [vp] * 8
+    L.ca_backward.restype = st
+    L.ca_backward.argtypes = [vp] * 12
+    L.ca_merge.restype = st
+    L.ca_merge.argtypes = [i32, vp, vp, i32, i64, i32, i32, vp, i32, vp, vp]
+    L.ca_device_status.restype = st
+    L.ca_device_status.argtypes = [vp, vp]
+    L.ca_plan_set_wait_limit.restype = st
+    L.ca_plan_set_wait_limit.argtypes = [vp, i64]
+    L.ca_watchdog_selftest.restype = st
+    L.ca_watchdog_selftest.argtypes = [vp, i64, vp]
+    L.ca_status_string.restype = ctypes.c_char_p
+    L.ca_status_string.argtypes = [st]
+    L.ca_last_error.restype = ctypes.c_char_p
+    L.ca_last_error.argtypes = []
+    L.ca_version.restype = i32
+    L.ca_version.argtypes = []
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != CA_OK:
+        L = load()
+        raise CAError(status, f"{L.ca_status_string(status).decode()}: {L.ca_last_error().decode()}")
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len):
+    n = len(task_q_len)
+    arr = (Task * max(n, 1))()
+    for i in range(n):
+        arr[i].doc_id = int(task_doc[i])
+        arr[i].reserved = 0
+        arr[i].q_start = int(task_q_start[i])
+        arr[i].q_len = int(task_q_len[i])
+        arr[i].kv_start = int(task_kv_start[i])
+        arr[i].kv_len = int(task_kv_len[i])
+    return arr, n
+
+
+def dry_run(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len, doc_len, doc_kv_offset,
+            num_q_heads: int, num_kv_heads: int, head_dim: int, softmax_scale: Optional[float] = None,
+            o_dtype: int = CA_DTYPE_BF16):
+    """ca_plan_dry_run: validation and integer accounting without a device.
+    Returns (info dict, per-task pairs)."""
+    L = load()
+    arr, n = _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len)
+    dl = np.ascontiguousarray(doc_len, dtype=np.int64)
+    do = np.ascontiguousarray(doc_kv_offset, dtype=np.int64)
+    if softmax_scale is None:
+        softmax_scale = head_dim ** -0.5
+    shape = Shape(num_q_heads, num_kv_heads, head_dim, float(softmax_scale), int(o_dtype))
+    info = PlanInfo()
+    pairs = np.zeros(max(n, 1), dtype=np.int64)
+    _check(L.ca_plan_dry_run(arr, n, dl.ctypes.data, do.ctypes.data, len(dl), ctypes.byref(shape),
+                             ctypes.byref(info), pairs.ctypes.data))
+    return info.as_dict(), pairs[:n]
+
+
+def dry_run_workload(w):
+    return dry_run(w.task_doc, w.task_q_start, w.task_q_len, w.task_kv_start, w.task_kv_len, w.doc_len,
+                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale)
+
+
+class Plan:
+    """A validated CA-task pool uploaded to the current device (ca_plan_create)."""
+
+    def __init__(self, task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len, doc_len, doc_kv_offset,
+                 num_q_heads: int, num_kv_heads: int, head_dim: int, softmax_scale: Optional[float] = None,
+                 o_dtype: int = CA_DTYPE_BF16, stream=None):
+        L = load()
+        arr, n = _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len)
+        self._doc_len = np.ascontiguousarray(doc_len, dtype=np.int64)
+        self._doc_off = np.ascontiguousarray(doc_kv_offset, dtype=np.int64)
+        if softmax_scale is None:
+            softmax_scale = head_dim ** -0.5
+        shape = Shape(num_q_heads, num_kv_heads, head_dim, float(softmax_scale), int(o_dtype))
+        h = ctypes.c_void_p()
+        _check(L.ca_plan_create(arr, n, self._doc_len.ctypes.data, self._doc_off.ctypes.data,
+                                len(self._doc_len), ctypes.byref(shape), _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
+        self.o_dtype = o_dtype
+        self.n_tasks = n
+
+    @classmethod
+    def from_workload(cls, w, o_dtype: int = CA_DTYPE_BF16, stream=None) -> "Plan":
+        return cls(w.task_doc, w.task_q_start, w.task_q_len, w.task_kv_start, w.task_kv_len, w.doc_len,
+                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale, o_dtype, stream)
+
+    @property
+    def handle(self) -> int:
+        if self._h is None or not self._h.value:
+            raise RuntimeError("plan is closed")
+        return self._h.value
+
+    def info(self) -> dict:
+        out = PlanInfo()
+        _check(load().ca_plan_info(self.handle, ctypes.byref(out)))
+        return out.as_dict()
+
+    def task_pairs(self) -> np.ndarray:
+        out = np.zeros(self.n_tasks, dtype=np.int64)
+        _check(load().ca_plan_task_pairs(self.handle, out.ctypes.data))
+        return out
+
+    def forward(self, q, k, v, o, lse, workspace=None, stream=None):
+        _check(load().ca_forward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                 _stream(stream)))
+
+    def backward(self, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=None):
+        _check(load().ca_backward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _stream(stream)))
+
+    def device_status(self, stream=None) -> int:
+        """Sync the stream and return (and clear) the device error status."""
+        return int(load().ca_device_status(self.handle, _stream(stream)))
+
+    def set_wait_limit(self, ns: int):
+        _check(load().ca_plan_set_wait_limit(self.handle, int(ns)))
+
+    def watchdog_selftest(self, limit_ns: int, stream=None):
+        _check(load().ca_watchdog_selftest(self.handle, int(limit_ns), _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().ca_plan_destroy(self._h.value)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def merge(o_parts: Sequence, lse_parts: Sequence, rows: int, heads: int, head_dim: int, o_out, lse_out=None,
+          parts_dtype: int = CA_DTYPE_FP32, out_dtype: int = CA_DTYPE_BF16, stream=None):
+    """ca_merge over n partial (O, LSE) results."""
+    n = len(o_parts)
+    op = (ctypes.c_void_p * n)(*[_ptr(x) for x in o_parts])
+    lp = (ctypes.c_void_p * n)(*[_ptr(x) for x in lse_parts])
+    _check(load().ca_merge(n, op, lp, int(parts_dtype), int(rows), int(heads), int(head_dim), _ptr(o_out),
+                           int(out_dtype), _ptr(lse_out), _stream(stream)))
+
+
+def version() -> int:
+    return int(load().ca_version())

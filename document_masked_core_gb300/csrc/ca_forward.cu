@@ -1,0 +1,448 @@
+// Forward core attention over a rebatched pool of CA-tasks (sm_103a).
+//
+// One persistent CTA per SM walks the plan's forward tiles (longest first).
+// A tile is 128 query rows = (128 / G tokens) x (G heads of one kv head g), so
+// one K/V tile of 128 keys of head g serves all 128 rows (GQA sharing by
+// packing heads into the MMA M dimension).  For each visible 128-key tile:
+//   S = Q K^T            tcgen05.mma, bf16 x bf16 -> fp32 in TMEM (2 buffers)
+//   online softmax       one thread per row reads its S row from TMEM, masks
+//                        the causal / block edges, keeps the running max m and
+//                        sum l (log2 domain), writes P as bf16 over S in TMEM
+//   O += P V             tcgen05.mma with A = P from TMEM, B = V (MN-major)
+// and finally O /= l, LSE = ln 2 (m + log2 l).  The online-softmax recurrence
+// with saved row statistics is the one the disaggregation paper relies on
+// (Efficient Long-context Language Model Training by Core Attention
+// Disaggregation, §3.4 "Property 1: Statelessness"); fully masked key tiles
+// are never visited (the plan lists only visible tiles).
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue (thread i <-> TMEM
+// lane i <-> tile row i), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
+#include <algorithm>
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "ca_sm100.cuh"
+
+namespace ca {
+namespace {
+
+using namespace dev;
+
+struct FwdParams {
+    const DevTask *tasks;
+    const FwdItem *items;
+    int32_t n_items;
+    int32_t hq, G, tpt;
+    float scale_log2;  // softmax_scale * log2(e)
+    void *o;
+    float *lse;
+    DevCtl ctl;
+};
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kStages = 2;
+    static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 64 bf16
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // 128 rows x D bf16
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    // + barriers + alignment slack; at least 120 KB so that one CTA (which
+    // owns all 512 TMEM columns) runs per SM
+    static constexpr int kSmemBytes = (kOffBar + 512 + 1024) > 122880 ? (kOffBar + 512 + 1024) : 122880;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;    // S/P buffers at 0 and 128
+    static constexpr uint32_t kColO = 256;  // O accumulator, D columns
+    static constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+};
+
+struct FwdBars {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t s_full[2], p_full[2];
+    uint64_t o_full, o_empty, mma_done;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+struct ItemGeo {
+    int32_t g, row0, p_first, ntok, kv_start, kv_end, kv_off, j_first, n_kv;
+};
+
+__device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) {
+    const FwdItem it = p.items[idx];
+    const DevTask t = p.tasks[it.task];
+    ItemGeo gi;
+    gi.g = it.g;
+    const int32_t tok0 = it.tile * p.tpt;
+    gi.row0 = t.row0 + tok0;
+    gi.p_first = t.q_start + tok0;
+    gi.ntok = min(p.tpt, t.q_len - tok0);
+    gi.kv_start = t.kv_start;
+    gi.kv_end = t.kv_start + t.kv_len;
+    gi.kv_off = t.kv_off;
+    const int32_t hi = min(gi.kv_end, gi.p_first + gi.ntok);  // exclusive
+    if (hi <= gi.kv_start) {
+        gi.j_first = 0;
+        gi.n_kv = 0;
+    } else {
+        gi.j_first = gi.kv_start / kTileKeys;
+        gi.n_kv = (hi - 1) / kTileKeys - gi.j_first + 1;
+    }
+    return gi;
+}
+
+// Make the compiler treat the 32 registers as produced after the preceding
+// tcgen05.wait::ld (their values are only valid after it).
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(192, 1)
+    ca_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sK = smem + C::kOffK;
+    uint8_t *sV = smem + C::kOffV;
+    FwdBars &bars = *reinterpret_cast<FwdBars *>(smem + C::kOffBar);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.s_full[b], 1);
+            mbar_init(&bars.p_full[b], 128);
+        }
+        mbar_init(&bars.o_full, 1);
+        mbar_init(&bars.o_empty, 128);
+        mbar_init(&bars.mma_done, 1);
+        bars.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&bars.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    const Watchdog wd{&p.ctl, &bars.abort_flag};
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, act = 0;
+            bool ok = true;
+            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+                const ItemGeo gi = decode_item(p, idx);
+                if (gi.n_kv == 0) continue;
+                if (!(ok = mbar_wait(&bars.q_empty, (act & 1) ^ 1, wd))) break;
+                mbar_arrive_expect_tx(&bars.q_full, C::kTileBytes);
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d(sQ + h * C::kHalfBytes, &tm_q, &bars.q_full, h * 64, gi.g * p.G, gi.row0);
+                for (int32_t i = 0; i < gi.n_kv; ++i, ++kv_it) {
+                    const uint32_t st = kv_it % C::kStages;
+                    const uint32_t ph = (kv_it / C::kStages) & 1;
+                    if (!(ok = mbar_wait(&bars.kv_empty[st], ph ^ 1, wd))) break;
+                    const int32_t key_row = gi.kv_off + (gi.j_first + i) * kTileKeys;
+                    mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        tma_load_3d(sK + st * C::kTileBytes + h * C::kHalfBytes, &tm_k, &bars.k_full[st], h * 64,
+                                    gi.g, key_row);
+                    mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        tma_load_3d(sV + st * C::kTileBytes + h * C::kHalfBytes, &tm_v, &bars.v_full[st], h * 64,
+                                    gi.g, key_row);
+                }
+                ++act;
+            }
+            if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kv_it = 0, s_it = 0, act = 0;
+            bool ok = true;
+            const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+            auto issue_s = [&](uint32_t kv_idx, uint32_t s_idx) -> bool {
+                const uint32_t st = kv_idx % C::kStages;
+                if (!mbar_wait(&bars.k_full[st], (kv_idx / C::kStages) & 1, wd)) return false;
+                tc_fence_after();
+                const uint32_t b = s_idx & 1;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                    const uint64_t ad = sdesc_sw128(q_base + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(k_base + st * C::kTileBytes + off, 16, 1024);
+                    umma_ss(tmem + C::kColS + b * 128, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&bars.s_full[b]);
+                return true;
+            };
+            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+                const ItemGeo gi = decode_item(p, idx);
+                if (gi.n_kv == 0) continue;
+                if (!(ok = mbar_wait(&bars.q_full, act & 1, wd))) break;
+                tc_fence_after();
+                if (!(ok = issue_s(kv_it, s_it))) break;
+                for (int32_t i = 0; i < gi.n_kv && ok; ++i) {
+                    if (i + 1 < gi.n_kv && !(ok = issue_s(kv_it + i + 1, s_it + i + 1))) break;
+                    const uint32_t si = s_it + i;
+                    const uint32_t b = si & 1;
+                    if (!(ok = mbar_wait(&bars.p_full[b], (si >> 1) & 1, wd))) break;
+                    const uint32_t kvi = kv_it + i;
+                    const uint32_t st = kvi % C::kStages;
+                    if (!(ok = mbar_wait(&bars.v_full[st], (kvi / C::kStages) & 1, wd))) break;
+                    if (i == 0 && !(ok = mbar_wait(&bars.o_empty, (act & 1) ^ 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bd = sdesc_sw128(v_base + st * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
+                        umma_ts(tmem + C::kColO, tmem + C::kColS + b * 128 + kk * 8, bd, C::kIdescPV,
+                                (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bars.kv_empty[st]);
+                    umma_commit(&bars.o_full);
+                }
+                if (!ok) break;
+                umma_commit(&bars.q_empty);
+                kv_it += gi.n_kv;
+                s_it += gi.n_kv;
+                ++act;
+            }
+            // every MMA issued above has completed once this arrives
+            umma_commit(&bars.mma_done);
+            const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
+            uint32_t zero = 0;
+            const Watchdog wd2{&drain, &zero};
+            mbar_wait(&bars.mma_done, 0, wd2);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const uint32_t row = threadIdx.x;  // 0..127
+        const uint32_t lane_addr = (warp * 32u) << 16;
+        uint32_t s_it = 0;
+        bool ok = true;
+        for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            const ItemGeo gi = decode_item(p, idx);
+            const int32_t tok = row / p.G;
+            const int32_t h = gi.g * p.G + (row % p.G);
+            const bool valid = tok < gi.ntok;
+            const int32_t pos = gi.p_first + min(tok, gi.ntok - 1);
+            const int32_t kv_lo = gi.kv_start;
+            const int32_t kv_hi = min(gi.kv_end, pos + 1);
+            const size_t out_idx = (static_cast<size_t>(gi.row0 + tok) * p.hq + h);
+            if (gi.n_kv == 0) {
+                if (valid) {
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D);
+#pragma unroll
+                        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D);
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                    }
+                    p.lse[out_idx] = -INFINITY;
+                }
+                continue;
+            }
+            float m = -INFINITY, l = 0.f;
+            for (int32_t i = 0; i < gi.n_kv; ++i) {
+                const uint32_t si = s_it + i;
+                const uint32_t b = si & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[b], (si >> 1) & 1, wd));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[4][32];
+                const uint32_t s_addr = tmem + lane_addr + C::kColS + b * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+                const int32_t key0 = (gi.j_first + i) * kTileKeys;
+                const bool need_mask = key0 < kv_lo || key0 + kTileKeys > kv_hi;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float v = __uint_as_float(sr[c][e]) * p.scale_log2;
+                        if (need_mask) {
+                            const int32_t key = key0 + c * 32 + e;
+                            if (key < kv_lo || key >= kv_hi) v = -INFINITY;
+                        }
+                        sr[c][e] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+                }
+                const float m_new = fmaxf(m, mx);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m - m_use);
+                float sum = 0.f;
+                uint32_t pk[2][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2(__uint_as_float(sr[c][e]) - m_use);
+                        const float p1 = ex2(__uint_as_float(sr[c][e + 1]) - m_use);
+                        sum += p0 + p1;
+                        pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
+                    }
+                }
+                l = l * alpha + sum;
+                tmem_st32(s_addr, pk[0]);
+                tmem_st32(s_addr + 32, pk[1]);
+                if (i > 0) {
+                    // rescale the O accumulated so far once PV_{i-1} has landed
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full, (si - 1) & 1, wd));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
+                        const uint32_t o_addr = tmem + lane_addr + C::kColO;
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t orr[32];
+                            tmem_ld32(o_addr + c * 32, orr);
+                            tmem_ld_wait();
+                            reg_fence(orr);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                            tmem_st32(o_addr + c * 32, orr);
+                        }
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.p_full[b]);
+                m = m_new;
+            }
+            if (!ok) break;
+            // epilogue: O / l and LSE
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full, (s_it + gi.n_kv - 1) & 1, wd));
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const uint32_t o_addr = tmem + lane_addr + C::kColO;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(o_addr + c * 32, orr);
+                tmem_ld_wait();
+                reg_fence(orr);
+                if (valid) {
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(orr[4 * e]) * inv_l,
+                                                 __uint_as_float(orr[4 * e + 1]) * inv_l,
+                                                 __uint_as_float(orr[4 * e + 2]) * inv_l,
+                                                 __uint_as_float(orr[4 * e + 3]) * inv_l);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(orr[8 * e + 0]) * inv_l, __uint_as_float(orr[8 * e + 1]) * inv_l);
+                            w.y = pack_bf16(__uint_as_float(orr[8 * e + 2]) * inv_l, __uint_as_float(orr[8 * e + 3]) * inv_l);
+                            w.z = pack_bf16(__uint_as_float(orr[8 * e + 4]) * inv_l, __uint_as_float(orr[8 * e + 5]) * inv_l);
+                            w.w = pack_bf16(__uint_as_float(orr[8 * e + 6]) * inv_l, __uint_as_float(orr[8 * e + 7]) * inv_l);
+                            dst[e] = w;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.o_empty);
+            if (valid) p.lse[out_idx] = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+            s_it += gi.n_kv;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool F32>
+cudaError_t launch_fwd_t(const ca_plan *pl, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const FwdParams &prm, cudaStream_t stream) {
+    using C = FwdCfg<D>;
+    auto kern = ca_fwd_kernel<D, F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<int64_t>(pl->n_fwd, pl->num_sms));
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, const void *v, void *o, float *lse,
+                           cudaStream_t stream) {
+    if (pl->n_fwd == 0) return cudaSuccess;
+    CUtensorMap tq, tk, tv;
+    if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
+        make_tmap_3d(&tk, k, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK ||
+        make_tmap_3d(&tv, v, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK)
+        return cudaErrorInvalidValue;
+    FwdParams prm;
+    prm.tasks = pl->d_tasks;
+    prm.items = pl->d_fwd;
+    prm.n_items = static_cast<int32_t>(pl->n_fwd);
+    prm.hq = pl->hq;
+    prm.G = pl->G;
+    prm.tpt = pl->tpt;
+    prm.scale_log2 = pl->scale * 1.4426950408889634f;
+    prm.o = o;
+    prm.lse = lse;
+    prm.ctl.err = pl->d_err;
+    prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
+    const bool f32 = pl->o_dtype == CA_DTYPE_FP32;
+    if (pl->d == 128)
+        return f32 ? launch_fwd_t<128, true>(pl, tq, tk, tv, prm, stream)
+                   : launch_fwd_t<128, false>(pl, tq, tk, tv, prm, stream);
+    return f32 ? launch_fwd_t<64, true>(pl, tq, tk, tv, prm, stream)
+               : launch_fwd_t<64, false>(pl, tq, tk, tv, prm, stream);
+}
+
+}  // namespace ca

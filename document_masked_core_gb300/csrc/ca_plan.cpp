@@ -1,0 +1,470 @@
+// Host side of the C ABI: argument validation, integer accounting, the
+// forward/backward tile lists (longest first), device upload, tensor maps and
+// the entry points declared in include/ca.h.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "ca_internal.h"
+
+namespace ca {
+
+namespace {
+thread_local std::string g_last_error;
+
+// Pairs of one task: sum over rows p in [q0, q0 + ql) of
+// |{j : a <= j < e, j <= p}|, by splitting the rows into the ramp
+// a <= p < e - 1 (p - a + 1 keys) and the plateau p >= e - 1 (e - a keys).
+int64_t task_pairs_closed_form(int64_t q0, int64_t ql, int64_t a, int64_t kl) {
+    const int64_t e = a + kl;
+    const int64_t q1 = q0 + ql;  // exclusive
+    int64_t total = 0;
+    const int64_t r0 = std::max(q0, a), r1 = std::min(q1, e - 1);
+    if (r1 > r0) {
+        // sum_{p=r0}^{r1-1} (p - a + 1)
+        const int64_t first = r0 - a + 1, last = r1 - 1 - a + 1, n = r1 - r0;
+        total += (first + last) * n / 2;
+    }
+    const int64_t s0 = std::max(q0, e - 1);
+    if (q1 > s0) total += (q1 - s0) * kl;
+    return total;
+}
+
+// Forward tile geometry, mirrored by the kernel's decode.
+int32_t fwd_tile_nkv(const DevTask &t, int32_t tile, int32_t tpt) {
+    const int32_t tok0 = tile * tpt;
+    const int32_t ntok = std::min(tpt, t.q_len - tok0);
+    const int32_t hi = std::min(t.kv_start + t.kv_len, t.q_start + tok0 + ntok);
+    if (hi <= t.kv_start) return 0;
+    return (hi - 1) / kTileKeys - t.kv_start / kTileKeys + 1;
+}
+
+// Query tiles of task t that see key tile jt (mirrored by the backward kernel):
+// rows p >= max(128 jt, kv_start) of the task, provided the key tile
+// intersects the task's block.  Returns the first tile and the count.
+void bwd_task_tiles(const DevTask &t, int32_t jt, int32_t tpt, int32_t *first, int32_t *count) {
+    const int32_t k0 = jt * kTileKeys, k1 = k0 + kTileKeys;
+    const int32_t a = t.kv_start, e = t.kv_start + t.kv_len;
+    *first = 0;
+    *count = 0;
+    if (k1 <= a || k0 >= e) return;
+    const int32_t pmin = std::max(k0, a);
+    const int32_t q1 = t.q_start + t.q_len;
+    if (pmin >= q1) return;
+    const int32_t r = std::max(pmin, t.q_start) - t.q_start;
+    *first = r / tpt;
+    *count = (t.q_len - 1) / tpt - *first + 1;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+
+ca_status_t fail(ca_status_t st, const std::string &msg) {
+    g_last_error = msg;
+    return st;
+}
+
+ca_status_t cuda_fail(cudaError_t e, const char *what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return CA_ERR_CUDA;
+}
+
+ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32_t heads, int32_t dim,
+                         int32_t box_heads, int32_t box_rows) {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q{};
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(CA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t gdim[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
+    cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(heads) * dim * 2};
+    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CA_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(r) + ")");
+    return CA_OK;
+}
+
+}  // namespace ca
+
+using namespace ca;
+
+namespace {
+
+template <typename T>
+cudaError_t upload(T **dst, const std::vector<T> &src, cudaStream_t s) {
+    *dst = nullptr;
+    if (src.empty()) return cudaSuccess;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(dst), src.size() * sizeof(T));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, s);
+}
+
+void free_device(ca_plan *p) {
+    cudaFree(p->d_tasks);
+    cudaFree(p->d_fwd);
+    cudaFree(p->d_bwd);
+    cudaFree(p->d_doc_task_ptr);
+    cudaFree(p->d_doc_tasks);
+    cudaFree(p->d_doc_info);
+    cudaFree(p->d_err);
+    p->d_tasks = nullptr;
+    p->d_fwd = nullptr;
+    p->d_bwd = nullptr;
+    p->d_doc_task_ptr = nullptr;
+    p->d_doc_tasks = nullptr;
+    p->d_doc_info = nullptr;
+    p->d_err = nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kI32Max = 2147483647LL;
+
+}  // namespace
+
+extern "C" {
+
+int32_t ca_version(void) { return (1 << 16) | 0; }
+
+const char *ca_status_string(ca_status_t s) {
+    switch (s) {
+        case CA_OK: return "ok";
+        case CA_ERR_INVALID_ARG: return "invalid argument";
+        case CA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CA_ERR_CUDA: return "CUDA error";
+        case CA_ERR_DEVICE_TIMEOUT: return "device wait limit exceeded";
+        case CA_ERR_DEVICE_BOUNDS: return "device index check failed";
+        case CA_ERR_NO_DEVICE: return "no sm_103 device";
+    }
+    return "unknown status";
+}
+
+const char *ca_last_error(void) { return g_last_error.c_str(); }
+
+namespace {
+
+struct HostPlan {
+    ca_plan *p = nullptr;
+    std::vector<FwdItem> fwd;
+    std::vector<BwdItem> bwd;
+    std::vector<int32_t> ptr, dtasks, doc_info;
+};
+
+// Validation and all integer work of a plan; touches no device.
+ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
+                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape, HostPlan *hp) {
+    if (!tasks || !doc_len || !doc_kv_offset || !shape) return fail(CA_ERR_INVALID_ARG, "NULL argument");
+    if (n_tasks < 1) return fail(CA_ERR_INVALID_ARG, "n_tasks must be >= 1");
+    if (n_docs < 1) return fail(CA_ERR_INVALID_ARG, "n_docs must be >= 1");
+    const ca_shape_t sh = *shape;
+    if (sh.num_q_heads < 1 || sh.num_kv_heads < 1 || sh.num_q_heads % sh.num_kv_heads != 0)
+        return fail(CA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+    if (!(sh.softmax_scale > 0.f) || !std::isfinite(sh.softmax_scale))
+        return fail(CA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+    if (sh.o_dtype != CA_DTYPE_BF16 && sh.o_dtype != CA_DTYPE_FP32)
+        return fail(CA_ERR_INVALID_ARG, "o_dtype must be CA_DTYPE_BF16 or CA_DTYPE_FP32");
+    if (sh.head_dim != 64 && sh.head_dim != 128) return fail(CA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    const int32_t G = sh.num_q_heads / sh.num_kv_heads;
+    if (G > kTileRows || kTileRows % G != 0)
+        return fail(CA_ERR_UNSUPPORTED, "num_q_heads / num_kv_heads must divide 128");
+
+    // documents: non-negative, non-overlapping KV ranges
+    std::vector<std::pair<int64_t, int64_t>> ranges(n_docs);
+    int64_t total_kv = 0;
+    for (int32_t i = 0; i < n_docs; ++i) {
+        if (doc_len[i] < 1 || doc_kv_offset[i] < 0)
+            return fail(CA_ERR_INVALID_ARG, "document " + std::to_string(i) + " has a bad length or offset");
+        if (doc_len[i] > kI32Max || doc_kv_offset[i] + doc_len[i] > kI32Max)
+            return fail(CA_ERR_INVALID_ARG, "document rows must stay below 2^31");
+        ranges[i] = {doc_kv_offset[i], doc_kv_offset[i] + doc_len[i]};
+        total_kv = std::max(total_kv, doc_kv_offset[i] + doc_len[i]);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (int32_t i = 1; i < n_docs; ++i)
+        if (ranges[i].first < ranges[i - 1].second) return fail(CA_ERR_INVALID_ARG, "document KV ranges overlap");
+
+    ca_plan *p = new (std::nothrow) ca_plan();
+    if (!p) return fail(CA_ERR_INVALID_ARG, "out of host memory");
+    hp->p = p;
+    p->n_tasks = n_tasks;
+    p->n_docs = n_docs;
+    p->hq = sh.num_q_heads;
+    p->hkv = sh.num_kv_heads;
+    p->d = sh.head_dim;
+    p->G = G;
+    p->tpt = kTileRows / G;
+    p->scale = sh.softmax_scale;
+    p->o_dtype = sh.o_dtype;
+    p->total_kv = total_kv;
+    p->task_pairs.resize(n_tasks);
+    p->h_tasks.resize(n_tasks);
+
+    int64_t row0 = 0;
+    for (int32_t t = 0; t < n_tasks; ++t) {
+        const ca_task_t &T = tasks[t];
+        const std::string tn = "task " + std::to_string(t) + ": ";
+        if (T.reserved != 0) return fail(CA_ERR_INVALID_ARG, tn + "reserved field must be 0");
+        if (T.doc_id < 0 || T.doc_id >= n_docs) return fail(CA_ERR_INVALID_ARG, tn + "unknown doc_id");
+        const int64_t L = doc_len[T.doc_id];
+        if (T.q_len < 1 || T.kv_len < 1) return fail(CA_ERR_INVALID_ARG, tn + "q_len and kv_len must be >= 1");
+        if (T.q_start < 0 || T.kv_start < 0) return fail(CA_ERR_INVALID_ARG, tn + "negative start");
+        if (T.q_start + T.q_len > L) return fail(CA_ERR_INVALID_ARG, tn + "query shard runs past the document");
+        if (T.kv_start + T.kv_len > L) return fail(CA_ERR_INVALID_ARG, tn + "KV block runs past the document");
+        if (row0 + T.q_len > kI32Max) return fail(CA_ERR_INVALID_ARG, "total query rows must stay below 2^31");
+        DevTask &d = p->h_tasks[t];
+        d.row0 = static_cast<int32_t>(row0);
+        d.q_start = static_cast<int32_t>(T.q_start);
+        d.q_len = static_cast<int32_t>(T.q_len);
+        d.kv_start = static_cast<int32_t>(T.kv_start);
+        d.kv_len = static_cast<int32_t>(T.kv_len);
+        d.doc = T.doc_id;
+        d.kv_off = static_cast<int32_t>(doc_kv_offset[T.doc_id]);
+        d.doc_len = static_cast<int32_t>(L);
+        p->task_pairs[t] = task_pairs_closed_form(T.q_start, T.q_len, T.kv_start, T.kv_len);
+        p->pairs += p->task_pairs[t];
+        row0 += T.q_len;
+    }
+    p->total_q = row0;
+
+    // forward tiles: (task, kv head, query tile), longest first
+    std::vector<FwdItem> &fwd = hp->fwd;
+    for (int32_t t = 0; t < n_tasks; ++t) {
+        const DevTask &d = p->h_tasks[t];
+        const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
+        for (int32_t tile = 0; tile < ntiles; ++tile) {
+            const int32_t nkv = fwd_tile_nkv(d, tile, p->tpt);
+            for (int32_t g = 0; g < p->hkv; ++g) fwd.push_back({t, g, tile, nkv});
+            p->fwd_tile_pairs += static_cast<int64_t>(nkv) * p->hkv;
+        }
+    }
+    std::stable_sort(fwd.begin(), fwd.end(), [](const FwdItem &a, const FwdItem &b) { return a.n_kv > b.n_kv; });
+    p->n_fwd = static_cast<int64_t>(fwd.size());
+
+    // documents -> tasks (CSR), and backward tiles: (document, kv head, key tile)
+    std::vector<int32_t> &ptr = hp->ptr, &dtasks = hp->dtasks, &doc_info = hp->doc_info;
+    ptr.assign(n_docs + 1, 0);
+    dtasks.assign(n_tasks, 0);
+    for (int32_t t = 0; t < n_tasks; ++t) ptr[tasks[t].doc_id + 1]++;
+    for (int32_t i = 0; i < n_docs; ++i) ptr[i + 1] += ptr[i];
+    {
+        std::vector<int32_t> fill(ptr.begin(), ptr.end() - 1);
+        for (int32_t t = 0; t < n_tasks; ++t) dtasks[fill[tasks[t].doc_id]++] = t;
+    }
+    std::vector<BwdItem> &bwd = hp->bwd;
+    doc_info.assign(2 * n_docs, 0);
+    for (int32_t i = 0; i < n_docs; ++i) {
+        doc_info[2 * i] = static_cast<int32_t>(doc_kv_offset[i]);
+        doc_info[2 * i + 1] = static_cast<int32_t>(doc_len[i]);
+        const int32_t nkt = static_cast<int32_t>((doc_len[i] + kTileKeys - 1) / kTileKeys);
+        for (int32_t jt = 0; jt < nkt; ++jt) {
+            int32_t nq = 0;
+            for (int32_t k = ptr[i]; k < ptr[i + 1]; ++k) {
+                int32_t f, c;
+                bwd_task_tiles(p->h_tasks[dtasks[k]], jt, p->tpt, &f, &c);
+                nq += c;
+            }
+            for (int32_t g = 0; g < p->hkv; ++g) bwd.push_back({i, g, jt, nq});
+            p->bwd_tile_pairs += static_cast<int64_t>(nq) * p->hkv;
+        }
+    }
+    std::stable_sort(bwd.begin(), bwd.end(), [](const BwdItem &a, const BwdItem &b) { return a.n_q > b.n_q; });
+    p->n_bwd = static_cast<int64_t>(bwd.size());
+
+    // workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned
+    const int64_t rows_heads = p->total_q * p->hq;
+    const int64_t dq_bytes = (rows_heads * p->d * 4 + 255) / 256 * 256;
+    const int64_t d_bytes = (rows_heads * 4 + 255) / 256 * 256;
+    p->workspace_bytes = dq_bytes + d_bytes;
+    return CA_OK;
+}
+
+void fill_info(const ca_plan *p, ca_plan_info_t *o) {
+    o->total_q = p->total_q;
+    o->total_kv = p->total_kv;
+    o->n_tasks = p->n_tasks;
+    o->n_docs = p->n_docs;
+    o->causal_pairs = p->pairs;
+    o->flops_fwd = 4LL * p->d * p->hq * p->pairs;
+    o->flops_bwd = 8LL * p->d * p->hq * p->pairs;
+    o->workspace_bytes = p->workspace_bytes;
+    o->n_fwd_items = p->n_fwd;
+    o->n_bwd_items = p->n_bwd;
+    o->fwd_tile_pairs = p->fwd_tile_pairs;
+    o->bwd_tile_pairs = p->bwd_tile_pairs;
+}
+
+}  // namespace
+
+ca_status_t ca_plan_dry_run(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
+                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape,
+                            ca_plan_info_t *info, int64_t *task_pairs) {
+    if (!info) return fail(CA_ERR_INVALID_ARG, "info is NULL");
+    HostPlan hp;
+    ca_status_t st = build_host_plan(tasks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    if (st == CA_OK) {
+        fill_info(hp.p, info);
+        if (task_pairs) std::copy(hp.p->task_pairs.begin(), hp.p->task_pairs.end(), task_pairs);
+    }
+    delete hp.p;
+    return st;
+}
+
+ca_status_t ca_plan_create(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
+                           const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape,
+                           void *upload_stream, ca_plan_t **out) {
+    if (!out) return fail(CA_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    HostPlan hp;
+    ca_status_t st = build_host_plan(tasks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    if (st != CA_OK) {
+        delete hp.p;
+        return st;
+    }
+    ca_plan *p = hp.p;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDeviceProperties"); }
+    if (prop.major != 10 || prop.minor != 3) {
+        delete p;
+        return fail(CA_ERR_NO_DEVICE, "current device is sm_" + std::to_string(prop.major) +
+                                          std::to_string(prop.minor) + ", the kernels are built for sm_103a");
+    }
+    p->num_sms = prop.multiProcessorCount;
+    cudaStream_t s = static_cast<cudaStream_t>(upload_stream);
+    if ((e = upload(&p->d_tasks, p->h_tasks, s)) != cudaSuccess ||
+        (e = upload(&p->d_fwd, hp.fwd, s)) != cudaSuccess || (e = upload(&p->d_bwd, hp.bwd, s)) != cudaSuccess ||
+        (e = upload(&p->d_doc_task_ptr, hp.ptr, s)) != cudaSuccess ||
+        (e = upload(&p->d_doc_tasks, hp.dtasks, s)) != cudaSuccess ||
+        (e = upload(&p->d_doc_info, hp.doc_info, s)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void **>(&p->d_err), 16)) != cudaSuccess ||
+        (e = cudaMemsetAsync(p->d_err, 0, 16, s)) != cudaSuccess || (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+        free_device(p);
+        delete p;
+        return cuda_fail(e, "plan upload");
+    }
+    *out = p;
+    return CA_OK;
+}
+
+ca_status_t ca_plan_info(const ca_plan_t *p, ca_plan_info_t *o) {
+    if (!p || !o) return fail(CA_ERR_INVALID_ARG, "NULL argument");
+    fill_info(p, o);
+    return CA_OK;
+}
+
+ca_status_t ca_plan_task_pairs(const ca_plan_t *p, int64_t *out) {
+    if (!p || !out) return fail(CA_ERR_INVALID_ARG, "NULL argument");
+    std::copy(p->task_pairs.begin(), p->task_pairs.end(), out);
+    return CA_OK;
+}
+
+void ca_plan_destroy(ca_plan_t *p) {
+    if (!p) return;
+    cudaDeviceSynchronize();
+    free_device(p);
+    delete p;
+}
+
+ca_status_t ca_plan_set_wait_limit(ca_plan_t *p, int64_t ns) {
+    if (!p || ns < 0) return fail(CA_ERR_INVALID_ARG, "bad plan or limit");
+    p->wait_limit_ns = ns;
+    return CA_OK;
+}
+
+ca_status_t ca_forward(const ca_plan_t *p, const void *q, const void *k, const void *v, void *o, float *lse,
+                       void *workspace, void *stream) {
+    (void)workspace;
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    if (!q || !k || !v || !o || !lse) return fail(CA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return fail(CA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (o == q || o == k || o == v || static_cast<void *>(lse) == o)
+        return fail(CA_ERR_INVALID_ARG, "outputs alias inputs");
+    cudaError_t e = launch_forward(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return CA_OK;
+}
+
+ca_status_t ca_backward(const ca_plan_t *p, const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
+                        void *stream) {
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
+        return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    const void *ptrs[] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
+    for (const void *x : ptrs)
+        if (!aligned16(x)) return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (dq == dk || dq == dv || dk == dv) return fail(CA_ERR_INVALID_ARG, "gradient outputs alias");
+    cudaError_t e = launch_backward(p, q, k, v, o, lse, d_o, dq, dk, dv, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return CA_OK;
+}
+
+ca_status_t ca_merge(int32_t n_parts, const void *const *o_parts, const float *const *lse_parts, int32_t parts_dtype,
+                     int64_t rows, int32_t heads, int32_t head_dim, void *o_out, int32_t out_dtype, float *lse_out,
+                     void *stream) {
+    if (n_parts < 1 || n_parts > kMaxMergeParts) return fail(CA_ERR_INVALID_ARG, "n_parts must be in [1, 64]");
+    if (!o_parts || !lse_parts || !o_out) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    if (rows < 0 || heads < 1 || head_dim < 8 || head_dim > 256 || head_dim % 8 != 0)
+        return fail(CA_ERR_INVALID_ARG, "bad rows / heads / head_dim");
+    if ((parts_dtype != CA_DTYPE_BF16 && parts_dtype != CA_DTYPE_FP32) ||
+        (out_dtype != CA_DTYPE_BF16 && out_dtype != CA_DTYPE_FP32))
+        return fail(CA_ERR_INVALID_ARG, "bad dtype");
+    for (int32_t s = 0; s < n_parts; ++s) {
+        if (!o_parts[s] || !lse_parts[s]) return fail(CA_ERR_INVALID_ARG, "NULL part pointer");
+        if (!aligned16(o_parts[s]) || !aligned16(lse_parts[s]))
+            return fail(CA_ERR_INVALID_ARG, "part pointers must be 16-byte aligned");
+    }
+    if (!aligned16(o_out) || (lse_out && !aligned16(lse_out)))
+        return fail(CA_ERR_INVALID_ARG, "output pointers must be 16-byte aligned");
+    if (rows == 0) return CA_OK;
+    cudaError_t e = launch_merge(n_parts, o_parts, lse_parts, parts_dtype, rows, heads, head_dim, o_out, out_dtype,
+                                 lse_out, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return CA_OK;
+}
+
+ca_status_t ca_device_status(const ca_plan_t *p, void *stream) {
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, p->d_err, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "device status");
+    if (word == 0) return CA_OK;
+    e = cudaMemsetAsync(p->d_err, 0, sizeof(word), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "device status clear");
+    if (word & kErrTimeout) return fail(CA_ERR_DEVICE_TIMEOUT, "a kernel wait ran out of its limit");
+    return fail(CA_ERR_DEVICE_BOUNDS, "a kernel index check failed");
+}
+
+ca_status_t ca_watchdog_selftest(const ca_plan_t *p, int64_t limit_ns, void *stream) {
+    if (!p || limit_ns < 0) return fail(CA_ERR_INVALID_ARG, "bad plan or limit");
+    cudaError_t e = launch_watchdog_selftest(p, limit_ns, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "watchdog self-test launch");
+    return CA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+"""Host-side checks of libca.so that need no GPU: every symbol include/ca.h
+declares is exported, the integer accounting of the plan equals the oracle's
+enumeration bit-exactly, and invalid descriptors are rejected."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import document_masked_core_gb300 as ca
+from document_masked_core_gb300 import build, capi
+import oracle
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ca.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ca_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(capi.LIB_PATH)
+    names = declared_symbols()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(capi.EXPORTS) == names
+
+
+def test_status_strings_and_version():
+    L = capi.load()
+    for s in range(7):
+        assert L.ca_status_string(s)
+    assert ca.version() >> 16 == 1
+
+
+WORKLOADS = [W.tiny_chunk(), W.llama8b_chunk(), W.rebatched_pool(), W.long_context_chunk(),
+             W.split_kv_prefill(), W.split_kv_prefill(split=False),
+             W.custom("kv_blocks", [300], [(0, 200, 100, 0, 64), (0, 200, 100, 64, 200), (0, 5, 20, 100, 7)],
+                      4, 1, 128)]
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w.name)
+def test_pair_accounting_bit_exact(w):
+    info, pairs = ca.dry_run_workload(w)
+    ref = oracle.task_pairs(w)
+    assert np.array_equal(pairs, ref)
+    assert info["causal_pairs"] == int(ref.sum())
+    fwd, bwd = oracle.flops(w)
+    assert info["flops_fwd"] == fwd and info["flops_bwd"] == bwd
+    assert info["total_q"] == w.total_q and info["total_kv"] == w.total_kv
+
+
+def tile_pairs_reference(w):
+    """Visible (query tile, key tile) pairs by enumerating tiles: a query tile
+    (128/G tokens of one task) and a 128-key tile of the document meet when
+    some row of the tile sees some key of the tile."""
+    G = w.num_q_heads // w.num_kv_heads
+    T = 128 // G
+    n = 0
+    for t in range(w.n_tasks):
+        q0, ql = int(w.task_q_start[t]), int(w.task_q_len[t])
+        a, e = int(w.task_kv_start[t]), int(w.task_kv_start[t] + w.task_kv_len[t])
+        for tile in range((ql + T - 1) // T):
+            p_lo = q0 + tile * T
+            p_hi = min(q0 + ql, p_lo + T) - 1
+            L = int(w.doc_len[w.task_doc[t]])
+            for jt in range((L + 127) // 128):
+                k0, k1 = jt * 128, jt * 128 + 127
+                lo, hi = max(k0, a), min(k1, e - 1, p_hi)
+                n += hi >= lo
+    return n * w.num_kv_heads
+
+
+@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[-1], W.rebatched_pool(total_q=4096, doc_lo=1000,
+                                                                              doc_hi=3000, shard_lo=50,
+                                                                              shard_hi=700)],
+                         ids=lambda w: w.name)
+def test_tile_lists_cover_visible_tiles(w):
+    info, _ = ca.dry_run_workload(w)
+    ref = tile_pairs_reference(w)
+    assert info["fwd_tile_pairs"] == ref
+    assert info["bwd_tile_pairs"] == ref
+
+
+def test_invalid_descriptors_rejected():
+    base = dict(task_doc=[0], task_q_start=[0], task_q_len=[10], task_kv_start=[0], task_kv_len=[10],
+                doc_len=[10], doc_kv_offset=[0], num_q_heads=4, num_kv_heads=1, head_dim=64)
+    ca.dry_run(**base)
+    bad = [
+        dict(task_q_len=[0]),
+        dict(task_q_start=[5]),                 # runs past the document
+        dict(task_kv_len=[11]),
+        dict(task_kv_start=[-1]),
+        dict(task_doc=[1]),                     # unknown document
+        dict(num_q_heads=6, num_kv_heads=4),    # not a multiple
+        dict(doc_len=[10, 5], doc_kv_offset=[0, 8]),  # overlapping documents
+        dict(softmax_scale=-1.0),
+    ]
+    for b in bad:
+        kw = dict(base, **b)
+        with pytest.raises(ca.CAError) as ei:
+            ca.dry_run(**kw)
+        assert ei.value.status == capi.CA_ERR_INVALID_ARG, b
+    for b in (dict(head_dim=96), dict(num_q_heads=3, num_kv_heads=1)):
+        with pytest.raises(ca.CAError) as ei:
+            ca.dry_run(**dict(base, **b))
+        assert ei.value.status == capi.CA_ERR_UNSUPPORTED, b
