@@ -1,9 +1,635 @@
-// Backward core attention (placeholder until the tcgen05 kernels land).
+// Backward core attention over a rebatched pool of CA-tasks (sm_103a), with
+// recompute: only LSE is kept from the forward (Efficient Long-context
+// Language Model Training by Core Attention Disaggregation, §3.4
+// "Property 1: Statelessness"; §3.2 "Information flow (backward pass)").
+//
+// Three launches:
+//   1. preprocess   D_p = dO_p . O_p per (row, head); zero the fp32 dQ
+//                   accumulator.  Memory-bound.
+//   2. main         one persistent CTA per SM walks (document, kv head g,
+//                   128-key tile) items, longest first.  K and V of the tile
+//                   stay in shared memory; the CTA loops over every query tile
+//                   (of every task of the document) that sees the key tile:
+//                     S^T  = K Q^T          tcgen05, fp32 in TMEM
+//                     dP^T = V dO^T         tcgen05, fp32 in TMEM
+//                     P^T  = exp(scale S^T - LSE), dS^T = scale P^T (dP^T - D)
+//                                           one thread per key row
+//                     dV  += P^T dO         A = P^T (bf16) from TMEM
+//                     dK  += dS^T Q         A = dS^T (bf16) from TMEM
+//                     dQ   = dS K           A = dS (bf16, MN-major) in smem
+//                   dK/dV accumulate in TMEM across all query tiles and all G
+//                   heads of the group (no atomics); dQ of each pair is added
+//                   to the fp32 accumulator with vector atomics.
+//   3. finalize     fp32 dQ -> bf16.
+#include <algorithm>
+#include <cmath>
+
+#include <cuda_bf16.h>
+
 #include "ca_sm100.cuh"
 
 namespace ca {
-cudaError_t launch_backward(const ca_plan *, const void *, const void *, const void *, const void *, const float *,
-                            const void *, void *, void *, void *, void *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+using namespace dev;
+
+// ------------------------------------------------------------------ preprocess
+template <bool O_F32>
+__global__ void __launch_bounds__(256) ca_bwd_pre_kernel(const void *o, const __nv_bfloat16 *d_o, float *D,
+                                                          float *dq_acc, int64_t units, int32_t d) {
+    const int32_t tpu = d / 8;  // 8 or 16 threads per (row, head), a power of two dividing 32
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t unit = gtid / tpu;
+    const int32_t part = static_cast<int32_t>(gtid % tpu);
+    float acc = 0.f;
+    if (unit < units) {
+        const int64_t elem = unit * d + part * 8;
+        const uint4 du = __ldg(reinterpret_cast<const uint4 *>(d_o + elem));
+        const uint32_t dw[4] = {du.x, du.y, du.z, du.w};
+        float ov[8];
+        if (O_F32) {
+            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(o) + elem);
+            const float4 a = __ldg(src), b = __ldg(src + 1);
+            ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+            ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
+        } else {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(o) + elem));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ov[2 * i] = __uint_as_float(w[i] << 16);
+                ov[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(__uint_as_float(dw[i] << 16), ov[2 * i], acc);
+            acc = fmaf(__uint_as_float(dw[i] & 0xFFFF0000u), ov[2 * i + 1], acc);
+        }
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + elem);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int off = tpu / 2; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off, tpu);
+    if (unit < units && part == 0) D[unit] = acc;
 }
+
+// ------------------------------------------------------------------ finalize
+__global__ void __launch_bounds__(256) ca_bwd_dq_kernel(const float *dq_acc, __nv_bfloat16 *dq, int64_t n8) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 *src = reinterpret_cast<const float4 *>(dq_acc) + 2 * i;
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    uint4 w;
+    w.x = pack_bf16(a.x, a.y);
+    w.y = pack_bf16(a.z, a.w);
+    w.z = pack_bf16(b.x, b.y);
+    w.w = pack_bf16(b.z, b.w);
+    reinterpret_cast<uint4 *>(dq)[i] = w;
+}
+
+// ------------------------------------------------------------------ main
+struct BwdParams {
+    const DevTask *tasks;
+    const BwdItem *items;
+    const int32_t *doc_task_ptr;
+    const int32_t *doc_tasks;
+    const int32_t *doc_info;  // {kv_off, doc_len} per document
+    int32_t n_items;
+    int32_t hq, hkv, G, tpt;
+    float scale;       // softmax scale
+    float scale_log2;  // softmax scale * log2(e)
+    const float *lse;  // [total_q, hq]
+    const float *Dvec; // [total_q, hq]
+    float *dq_acc;     // [total_q, hq, d]
+    __nv_bfloat16 *dk, *dv;
+    DevCtl ctl;
+};
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kHalfBytes = 128 * 128;
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;
+    static constexpr int kQStages = 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;
+    static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+    static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;  // dS, 128 keys x 128 q rows bf16
+    static constexpr int kOffRow = kOffDS + 2 * kHalfBytes;          // LSE2[2][128], D[2][128]
+    static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
+    static constexpr int kSmemRaw = kOffBar + 256 + 1024;
+    static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;     // S^T, then P^T (bf16); later dQ
+    static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16)
+    static constexpr uint32_t kColDV = 256;
+    static constexpr uint32_t kColDK = 256 + D;
+    static constexpr uint32_t kIdescST = idesc_bf16(128, 128, false, false);  // K-major x K-major
+    static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);    // TMEM A x MN-major B
+    static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
+};
+
+struct BwdBars {
+    uint64_t kv_full, kv_empty;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, mma_done;
+    uint64_t row_ready[2];
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+struct KvGeo {
+    int32_t doc, g, jt, n_q, kv_off, doc_len, t_begin, t_end;
+};
+
+__device__ __forceinline__ KvGeo decode_kv(const BwdParams &p, int32_t idx) {
+    const BwdItem it = p.items[idx];
+    KvGeo k;
+    k.doc = it.doc;
+    k.g = it.g;
+    k.jt = it.kv_tile;
+    k.n_q = it.n_q;
+    k.kv_off = p.doc_info[2 * it.doc];
+    k.doc_len = p.doc_info[2 * it.doc + 1];
+    k.t_begin = p.doc_task_ptr[it.doc];
+    k.t_end = p.doc_task_ptr[it.doc + 1];
+    return k;
+}
+
+// Query tiles of task t that see key tile jt (same rule as the host plan).
+__device__ __forceinline__ void task_tiles(const DevTask &t, int32_t jt, int32_t tpt, int32_t &first, int32_t &count) {
+    const int32_t k0 = jt * kTileKeys, k1 = k0 + kTileKeys;
+    const int32_t a = t.kv_start, e = t.kv_start + t.kv_len;
+    first = 0;
+    count = 0;
+    if (k1 <= a || k0 >= e) return;
+    const int32_t pmin = max(k0, a);
+    if (pmin >= t.q_start + t.q_len) return;
+    first = (max(pmin, t.q_start) - t.q_start) / tpt;
+    count = (t.q_len - 1) / tpt - first + 1;
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sK = smem + C::kOffK;
+    uint8_t *sV = smem + C::kOffV;
+    uint8_t *sQ = smem + C::kOffQ;
+    uint8_t *sDO = smem + C::kOffDO;
+    uint8_t *sDS = smem + C::kOffDS;
+    float *sLse = reinterpret_cast<float *>(smem + C::kOffRow);  // [2][128] (log2 domain)
+    float *sD = sLse + 256;                                        // [2][128]
+    BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::kOffBar);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars.kv_full, 1);
+        mbar_init(&bars.kv_empty, 1);
+        for (int s = 0; s < C::kQStages; ++s) {
+            mbar_init(&bars.q_full[s], 1);
+            mbar_init(&bars.q_empty[s], 1);
+        }
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.ds_full, 128);
+        mbar_init(&bars.dq_full, 1);
+        mbar_init(&bars.dq_empty, 128);
+        mbar_init(&bars.acc_empty, 128);
+        mbar_init(&bars.mma_done, 1);
+        mbar_init(&bars.row_ready[0], 128);
+        mbar_init(&bars.row_ready[1], 128);
+        bars.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&bars.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    const Watchdog wd{&p.ctl, &bars.abort_flag};
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t act = 0, qt = 0;
+            bool ok = true;
+            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+                const KvGeo kg = decode_kv(p, idx);
+                if (kg.n_q == 0) continue;
+                if (!(ok = mbar_wait(&bars.kv_empty, (act & 1) ^ 1, wd))) break;
+                const int32_t key_row = kg.kv_off + kg.jt * kTileKeys;
+                mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(sK + h * C::kHalfBytes, &tm_k, &bars.kv_full, h * 64, kg.g, key_row);
+                    tma_load_3d(sV + h * C::kHalfBytes, &tm_v, &bars.kv_full, h * 64, kg.g, key_row);
+                }
+                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                    const DevTask t = p.tasks[p.doc_tasks[k]];
+                    int32_t first, count;
+                    task_tiles(t, kg.jt, p.tpt, first, count);
+                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                        const uint32_t st = qt % C::kQStages;
+                        if (!(ok = mbar_wait(&bars.q_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd))) break;
+                        const int32_t qrow = t.row0 + tile * p.tpt;
+                        mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kTileBytes);
+#pragma unroll
+                        for (int h = 0; h < D / 64; ++h) {
+                            tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
+                                        h * 64, kg.g * p.G, qrow);
+                            tma_load_3d(sDO + st * C::kTileBytes + h * C::kHalfBytes, &tm_do, &bars.q_full[st],
+                                        h * 64, kg.g * p.G, qrow);
+                        }
+                    }
+                }
+                ++act;
+            }
+            if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t act = 0, qt = 0;
+            bool ok = true;
+            const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
+                           do_base = smem_u32(sDO), ds_base = smem_u32(sDS);
+            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+                const KvGeo kg = decode_kv(p, idx);
+                if (kg.n_q == 0) continue;
+                if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
+                bool first_tile = true;
+                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                    const DevTask t = p.tasks[p.doc_tasks[k]];
+                    int32_t first, count;
+                    task_tiles(t, kg.jt, p.tpt, first, count);
+                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                        const uint32_t st = qt % C::kQStages;
+                        if (!(ok = mbar_wait(&bars.q_full[st], (qt / C::kQStages) & 1, wd))) break;
+                        // dQ of the previous tile (aliasing S^T) has been read out
+                        if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
+                        tc_fence_after();
+                        const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
+                        // S^T = K Q^T, dP^T = V dO^T
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                            umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024),
+                                    sdesc_sw128(qb + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&bars.s_full);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                            umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                                    sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&bars.dp_full);
+                        // dV += P^T dO
+                        if (!(ok = mbar_wait(&bars.p_full, qt & 1, wd))) break;
+                        if (first_tile && !(ok = mbar_wait(&bars.acc_empty, (act & 1) ^ 1, wd))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                                    sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                    (first_tile && kk == 0) ? 0u : 1u);
+                        // dK += dS^T Q ; dQ = dS K
+                        if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                                    sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                    (first_tile && kk == 0) ? 0u : 1u);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ss(tmem + C::kColS, sdesc_sw128(ds_base + kk * 2048, C::kHalfBytes, 1024),
+                                    sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
+                                    kk > 0 ? 1u : 0u);
+                        umma_commit(&bars.dq_full);
+                        umma_commit(&bars.q_empty[st]);
+                        first_tile = false;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&bars.kv_empty);
+                ++act;
+            }
+            umma_commit(&bars.mma_done);
+            const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
+            uint32_t zero = 0;
+            const Watchdog wd2{&drain, &zero};
+            mbar_wait(&bars.mma_done, 0, wd2);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax-gradient warps
+        const uint32_t i = threadIdx.x;  // key row of S^T / dP^T lanes; q row of the dQ lanes
+        const uint32_t lane_addr = (warp * 32u) << 16;
+        uint32_t qt = 0;
+        bool ok = true;
+        for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            const KvGeo kg = decode_kv(p, idx);
+            const int32_t kpos = kg.jt * kTileKeys + static_cast<int32_t>(i);  // this thread's key
+            const bool key_in_doc = kpos < kg.doc_len;
+            const size_t key_out = (static_cast<size_t>(kg.kv_off) + kpos) * p.hkv + kg.g;
+            if (kg.n_q == 0) {
+                if (key_in_doc) {
+                    uint4 *a = reinterpret_cast<uint4 *>(p.dk + key_out * D);
+                    uint4 *b = reinterpret_cast<uint4 *>(p.dv + key_out * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        a[c] = make_uint4(0, 0, 0, 0);
+                        b[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                continue;
+            }
+            for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                const DevTask t = p.tasks[p.doc_tasks[k]];
+                int32_t first, count;
+                task_tiles(t, kg.jt, p.tpt, first, count);
+                const bool key_in_block = kpos >= t.kv_start && kpos < t.kv_start + t.kv_len;
+                for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                    const int32_t tok0 = tile * p.tpt;
+                    const int32_t ntok = min(p.tpt, t.q_len - tok0);
+                    const int32_t p_first = t.q_start + tok0;
+                    const int32_t qrow0 = t.row0 + tok0;
+                    // row statistics of this query tile (double-buffered by tile parity)
+                    float *lse_b = sLse + (qt & 1) * 128;
+                    float *d_b = sD + (qt & 1) * 128;
+                    {
+                        const int32_t tok = i / p.G;
+                        const int32_t h = kg.g * p.G + (i % p.G);
+                        float l2 = INFINITY, dd = 0.f;
+                        if (tok < ntok) {
+                            const size_t ix = static_cast<size_t>(qrow0 + tok) * p.hq + h;
+                            const float l = __ldg(p.lse + ix);
+                            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+                            dd = __ldg(p.Dvec + ix);
+                        }
+                        lse_b[i] = l2;
+                        d_b[i] = dd;
+                    }
+                    mbar_arrive(&bars.row_ready[qt & 1]);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_ready[qt & 1], (qt >> 1) & 1, wd));
+                    if (!ok) break;
+                    // visible rows for this key: tile rows r (token r / G) with
+                    // r_lo <= r < r_hi, i.e. p >= key position and the token inside the task
+                    const int32_t r_hi = ntok * p.G;
+                    const int32_t r_lo = key_in_block ? max(kpos - p_first, 0) * p.G : r_hi;
+                    // ---- P^T = exp(scale S^T - LSE), masked
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, qt & 1, wd));
+                    if (!ok) break;
+                    tc_fence_after();
+                    float pt[128];
+                    const uint32_t s_addr = tmem + lane_addr + C::kColS;
+                    {
+                        const float4 *l4 = reinterpret_cast<const float4 *>(lse_b);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t sr[32];
+                            tmem_ld32(s_addr + c * 32, sr);
+                            tmem_ld_wait();
+                            reg_fence(sr);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                const float4 lv = l4[(c * 32 + e) / 4];
+                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int r = c * 32 + e + u;
+                                    const float v = ex2(__uint_as_float(sr[e + u]) * p.scale_log2 - la[u]);
+                                    pt[r] = (r >= r_lo && r < r_hi) ? v : 0.f;
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int w = 0; w < 32; ++w) pk[w] = pack_bf16(pt[64 * m + 2 * w], pt[64 * m + 2 * w + 1]);
+                        tmem_st32(s_addr + 32 * m, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&bars.p_full);
+                    // ---- dS^T = scale P^T (dP^T - D): to TMEM (A of dK += dS^T Q) and to
+                    // shared memory as the MN-major A of dQ = dS K (key row i holds q rows
+                    // 0..63 in half 0 and 64..127 in half 1, 16-byte chunks swizzled by i % 8)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, qt & 1, wd));
+                    if (!ok) break;
+                    tc_fence_after();
+                    {
+                        const uint32_t dp_addr = tmem + lane_addr + C::kColDP;
+                        const float4 *d4 = reinterpret_cast<const float4 *>(d_b);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {  // q rows 32c .. 32c+31
+                            uint32_t dr[32];
+                            tmem_ld32(dp_addr + 32 * c, dr);
+                            tmem_ld_wait();
+                            reg_fence(dr);
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                const int r = 32 * c + e;
+                                const float4 dv4 = d4[r / 4];
+                                pk[e / 2] = pack_bf16(p.scale * pt[r] * (__uint_as_float(dr[e]) - dv4.x),
+                                                      p.scale * pt[r + 1] * (__uint_as_float(dr[e + 1]) - dv4.y));
+                                pk[e / 2 + 1] = pack_bf16(p.scale * pt[r + 2] * (__uint_as_float(dr[e + 2]) - dv4.z),
+                                                          p.scale * pt[r + 3] * (__uint_as_float(dr[e + 3]) - dv4.w));
+                            }
+                            // TMEM: q rows 32c.. packed two per column at column 16c
+                            tmem_st16(dp_addr + 16 * c, pk);
+                            uint8_t *row = sDS + (c >> 1) * C::kHalfBytes + i * 128;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int c8 = 4 * (c & 1) + j;  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
+                                *reinterpret_cast<uint4 *>(row + ((c8 ^ (i & 7)) * 16)) =
+                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            }
+                        }
+                        tmem_st_wait();
+                    }
+                    fence_view_async_shared();
+                    tc_fence_before();
+                    mbar_arrive(&bars.ds_full);
+                    // ---- dQ (lane i = q row i) -> fp32 accumulator
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, qt & 1, wd));
+                    if (!ok) break;
+                    tc_fence_after();
+                    {
+                        const int32_t tok = i / p.G;
+                        const int32_t h = kg.g * p.G + (i % p.G);
+                        float *dst = p.dq_acc + (static_cast<size_t>(qrow0 + tok) * p.hq + h) * D;
+                        const uint32_t q_addr = tmem + lane_addr + C::kColS;
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t qr[32];
+                            tmem_ld32(q_addr + c * 32, qr);
+                            tmem_ld_wait();
+                            reg_fence(qr);
+                            if (tok < ntok) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    atomicAdd(reinterpret_cast<float4 *>(dst + c * 32 + 4 * e),
+                                              make_float4(__uint_as_float(qr[4 * e]), __uint_as_float(qr[4 * e + 1]),
+                                                          __uint_as_float(qr[4 * e + 2]),
+                                                          __uint_as_float(qr[4 * e + 3])));
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&bars.dq_empty);
+                }
+            }
+            if (!ok) break;
+            // ---- epilogue: dK, dV of this key tile (lane i = key i); every MMA of
+            // the item completed before the last dq_full
+            {
+                const uint32_t dv_addr = tmem + lane_addr + C::kColDV;
+                const uint32_t dk_addr = tmem + lane_addr + C::kColDK;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(dv_addr + c * 32, a);
+                    tmem_ld32(dk_addr + c * 32, b);
+                    tmem_ld_wait();
+                    reg_fence(a);
+                    reg_fence(b);
+                    if (key_in_doc) {
+                        uint4 *va = reinterpret_cast<uint4 *>(p.dv + key_out * D + c * 32);
+                        uint4 *kb = reinterpret_cast<uint4 *>(p.dk + key_out * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            va[e] = make_uint4(pack_bf16(__uint_as_float(a[8 * e]), __uint_as_float(a[8 * e + 1])),
+                                               pack_bf16(__uint_as_float(a[8 * e + 2]), __uint_as_float(a[8 * e + 3])),
+                                               pack_bf16(__uint_as_float(a[8 * e + 4]), __uint_as_float(a[8 * e + 5])),
+                                               pack_bf16(__uint_as_float(a[8 * e + 6]), __uint_as_float(a[8 * e + 7])));
+                            kb[e] = make_uint4(pack_bf16(__uint_as_float(b[8 * e]), __uint_as_float(b[8 * e + 1])),
+                                               pack_bf16(__uint_as_float(b[8 * e + 2]), __uint_as_float(b[8 * e + 3])),
+                                               pack_bf16(__uint_as_float(b[8 * e + 4]), __uint_as_float(b[8 * e + 5])),
+                                               pack_bf16(__uint_as_float(b[8 * e + 6]), __uint_as_float(b[8 * e + 7])));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const CUtensorMap &tdo, const BwdParams &prm, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    auto kern = ca_bwd_main_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<int64_t>(pl->n_bwd, pl->num_sms));
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
+                            cudaStream_t stream) {
+    const int64_t units = pl->total_q * pl->hq;
+    float *dq_acc = static_cast<float *>(workspace);
+    float *Dvec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                            (units * pl->d * 4 + 255) / 256 * 256);
+    // 1. D = rowsum(dO * O), dQ accumulator = 0
+    {
+        const int64_t threads = units * (pl->d / 8);
+        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+        if (pl->o_dtype == CA_DTYPE_FP32)
+            ca_bwd_pre_kernel<true><<<blocks, 256, 0, stream>>>(o, static_cast<const __nv_bfloat16 *>(d_o), Dvec,
+                                                                dq_acc, units, pl->d);
+        else
+            ca_bwd_pre_kernel<false><<<blocks, 256, 0, stream>>>(o, static_cast<const __nv_bfloat16 *>(d_o), Dvec,
+                                                                 dq_acc, units, pl->d);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 2. main pass
+    CUtensorMap tq, tk, tv, tdo;
+    if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
+        make_tmap_3d(&tdo, d_o, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
+        make_tmap_3d(&tk, k, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK ||
+        make_tmap_3d(&tv, v, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK)
+        return cudaErrorInvalidValue;
+    BwdParams prm;
+    prm.tasks = pl->d_tasks;
+    prm.items = pl->d_bwd;
+    prm.doc_task_ptr = pl->d_doc_task_ptr;
+    prm.doc_tasks = pl->d_doc_tasks;
+    prm.doc_info = pl->d_doc_info;
+    prm.n_items = static_cast<int32_t>(pl->n_bwd);
+    prm.hq = pl->hq;
+    prm.hkv = pl->hkv;
+    prm.G = pl->G;
+    prm.tpt = pl->tpt;
+    prm.scale = pl->scale;
+    prm.scale_log2 = pl->scale * 1.4426950408889634f;
+    prm.lse = lse;
+    prm.Dvec = Dvec;
+    prm.dq_acc = dq_acc;
+    prm.dk = static_cast<__nv_bfloat16 *>(dk);
+    prm.dv = static_cast<__nv_bfloat16 *>(dv);
+    prm.ctl.err = pl->d_err;
+    prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
+    cudaError_t e = pl->d == 128 ? launch_main_t<128>(pl, tq, tk, tv, tdo, prm, stream)
+                                 : launch_main_t<64>(pl, tq, tk, tv, tdo, prm, stream);
+    if (e != cudaSuccess) return e;
+    // 3. dQ accumulator -> bf16
+    {
+        const int64_t n8 = units * pl->d / 8;
+        const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
+        ca_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n8);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
 }  // namespace ca
