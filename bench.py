@@ -1,0 +1,403 @@
+"""Benchmark of the document-masked core-attention hot path on GB300.
+
+One step = one forward (ca_forward) + one backward (ca_backward) of the
+rebatched CA-task pool over one synthetic 65536-token packed chunk shaped like
+a Llama-3-8B layer (32 query / 8 KV heads, head_dim 128, documents with
+lognormal lengths, median 2048, sigma 1.5, one CA-task per document; seed 0).
+The metric counts 12 * head_dim * H_q FLOPs per causal (token, key) pair:
+4 d forward and 8 d backward.
+
+Printed (rank 0, one JSON line): whole-job TFLOP/s over the timed steps with
+inputs resident in HBM (`value`), the same through the C ABI with host
+buffers (`e2e`: pinned host -> device copies of Q, K, V, dO and device -> host
+copies of dQ, dK, dV inside each timed step), the roofline of the dominant
+kernel (the backward main kernel, timed live with CUDA events on its stream),
+the clocks seen during the timed region, and the fp64 oracle timed on the host
+cores on a bounded sample of the same workload (`cpu_baseline`).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --impl reference the oracle itself is the measured arm: each step runs
+the oracle's forward + backward on a bounded sample (a prefix of the chunk's
+documents) on the host cores.  Under torchrun (N > 1) every rank runs an
+independent replica with its own seed (no data-path collective) and the
+slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "core-attention fwd+bwd TFLOP/s (causal-pair FLOPs), % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle sample
+
+def oracle_sample_workload(w, pair_budget: int, kv_groups: int = 1):
+    """Bounded sample of the chunk: its leading documents (at least one) whose
+    causal pairs per head stay within pair_budget, each one CA-task, with the
+    first ``kv_groups`` KV heads and their query heads."""
+    import workloads as W
+    lens = []
+    acc = 0
+    for L in w.doc_len:
+        p = int(L) * (int(L) + 1) // 2
+        if lens and acc + p > pair_budget:
+            break
+        lens.append(int(L))
+        acc += p
+    G = w.num_q_heads // w.num_kv_heads
+    return W.custom(f"{w.name}_prefix{len(lens)}_kv{kv_groups}", lens,
+                    [(i, 0, l, 0, l) for i, l in enumerate(lens)], G * kv_groups, kv_groups, w.head_dim,
+                    seed=w.seed)
+
+
+def time_oracle(ws, steps: int):
+    """Full fp64 oracle forward + backward on the sample workload, `steps`
+    times; returns (seconds per step, counted FLOPs per step)."""
+    import oracle
+    import workloads as W
+    q, k, v, do = W.make_tensors(ws, device="cpu")
+    pb = oracle.Problem(ws, q, k, v, do)
+    f, b = oracle.flops(ws)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.forward(pb)
+        oracle.backward(pb)
+        times.append(time.perf_counter() - t0)
+    return float(np.mean(times)), f + b
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    import oracle
+    import workloads as W
+    if rank != 0:
+        return
+    w = W.llama8b_chunk(seed=0)
+    ws = oracle_sample_workload(w, args.oracle_pairs // 2)
+    oracle.build()
+    t_warm, _ = time_oracle(ws, max(1, min(args.warmup, 1)))
+    t, flops = time_oracle(ws, args.steps)
+    value = flops / t / 1e12
+    sample = (f"{ws.n_docs} leading documents ({ws.total_q} tokens, {int(oracle.task_pairs(ws).sum())} causal "
+              f"pairs/head) of the chunk, {ws.num_q_heads} query heads sharing {ws.num_kv_heads} KV head(s), "
+              f"full fp64 forward + backward per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "seed": 0, "sample": ws.name},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    seed = args.seed + rank
+    w = W.llama8b_chunk(seed=seed)
+    q, k, v, do = W.make_tensors(w, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    t0 = time.perf_counter()
+    plan = ca.Plan.from_workload(w, stream=stream)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    info = plan.info()
+    ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    o, lse = ca.alloc_forward(plan, device=dev)
+    dq, dk, dv = ca.alloc_backward(plan, device=dev)
+    flops_step = info["flops_fwd"] + info["flops_bwd"]
+    sh = stream.cuda_stream
+
+    def step():
+        plan.forward(q, k, v, o, lse, ws, stream=sh)
+        plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws, stream=sh)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: inputs resident in HBM (Q, dO 512 MiB, K, V 128 MiB each: larger than L2)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for s in range(args.steps):
+            plan.set_timing_events(ev[s])
+            step()
+        end.record(stream)
+    stream.synchronize()
+    plan.set_timing_events(None)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the timed region")
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    value = flops_step * world / (ms * 1e-3) / 1e12
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    pre_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+    main_ms = float(np.mean([e[3].elapsed_time(e[4]) for e in ev]))
+    fin_ms = float(np.mean([e[4].elapsed_time(e[5]) for e in ev]))
+
+    # ---- end to end through the C ABI with host buffers
+    hq = q.cpu().pin_memory()
+    hk = k.cpu().pin_memory()
+    hv = v.cpu().pin_memory()
+    hdo = do.cpu().pin_memory()
+    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+    hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
+    hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    q2, k2, v2, do2 = (torch.empty_like(x) for x in (q, k, v, do))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dst, src in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
+                dst.copy_(src, non_blocking=True)
+            plan.forward(q2, k2, v2, o, lse, ws, stream=sh)
+            plan.backward(q2, k2, v2, o, lse, do2, dq_, dk_, dv_, ws, stream=sh)
+            for dst, src in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    stream.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world)
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the end-to-end region")
+
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+    main_tf = info["flops_bwd"] / (main_ms * 1e-3) / 1e12
+
+    line = None
+    if rank == 0:
+        # CPU baseline: the oracle on a bounded sample of the same workload
+        cpu = None
+        if not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            wsamp = oracle_sample_workload(w, args.oracle_pairs)
+            t_cpu, f_cpu = time_oracle(wsamp, 1)
+            cpu = {"value": f_cpu / t_cpu / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                   "sample": (f"{wsamp.n_docs} leading documents ({wsamp.total_q} tokens, "
+                              f"{int(oracle.task_pairs(wsamp).sum())} causal pairs/head) of the chunk, "
+                              f"{wsamp.num_q_heads} query heads sharing {wsamp.num_kv_heads} KV head(s), full "
+                              f"fp64 forward + backward; {t_cpu:.1f} s")}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": w.name, "seed": seed, "tokens": w.total_q, "documents": w.n_docs,
+                "heads": f"{w.num_q_heads}q/{w.num_kv_heads}kv", "head_dim": w.head_dim,
+                "causal_pairs_per_head": info["causal_pairs"], "flops_per_step": flops_step,
+                "flop_count": "12*head_dim*H_q*causal_pairs (4d forward + 8d backward)",
+                "l2": "inputs larger than L2 (Q and dO 512 MiB, K and V 128 MiB each)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "plan_ms": plan_ms,
+            },
+            "pct_of_peak": {"burst": 100.0 * value / world / peak, "sustained": 100.0 * value / world / peak_sus,
+                            "peaks": pk_kind},
+            "parts_ms": {"forward": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
+                         "bwd_dq_finalize": fin_ms},
+            "parts_tflops": {"forward": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12,
+                             "backward": info["flops_bwd"] / ((pre_ms + main_ms + fin_ms) * 1e-3) / 1e12},
+            "roofline": {"kernel": "ca_bwd_main_kernel", "bound": "tensor", "achieved": main_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": None,
+                         "peak_kind": f"bf16 burst, {pk_kind}",
+                         "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
+            "e2e": {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }
+    plan.close()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--oracle-pairs", type=int, default=8_000_000,
+                    help="causal pairs per head of the oracle's sample (bounds its CPU time)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        from document_masked_core_gb300 import build
+        if rank == 0:
+            build.build()
+        barrier(world)
+        line = run_gpu(args, rank, world, local)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

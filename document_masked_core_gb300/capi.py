@@ -30,7 +30,7 @@ CA_DTYPE_FP32 = 1
 EXPORTS = [
     "ca_plan_create", "ca_plan_dry_run", "ca_plan_info", "ca_plan_task_pairs", "ca_plan_destroy",
     "ca_forward", "ca_backward", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
-    "ca_watchdog_selftest", "ca_status_string", "ca_last_error", "ca_version",
+    "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
 ]
 
 
@@ -97,6 +97,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_plan_set_wait_limit.argtypes = [vp, i64]
     L.ca_watchdog_selftest.restype = st
     L.ca_watchdog_selftest.argtypes = [vp, i64, vp]
+    L.ca_plan_set_timing_events.restype = st
+    L.ca_plan_set_timing_events.argtypes = [vp, vp, i32]
     L.ca_status_string.restype = ctypes.c_char_p
     L.ca_status_string.argtypes = [st]
     L.ca_last_error.restype = ctypes.c_char_p
@@ -227,6 +229,16 @@ class Plan:
 
     def watchdog_selftest(self, limit_ns: int, stream=None):
         _check(load().ca_watchdog_selftest(self.handle, int(limit_ns), _stream(stream)))
+
+    def set_timing_events(self, events):
+        """Bracket each kernel launch with the given 6 torch.cuda.Events (or None)."""
+        if events is None:
+            self._events_arr = None
+            _check(load().ca_plan_set_timing_events(self.handle, None, 0))
+            return
+        arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
+        self._events_arr = (arr, list(events))  # keep the array and the events alive
+        _check(load().ca_plan_set_timing_events(self.handle, arr, len(events)))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -118,8 +118,11 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;  // dS, 128 keys x 128 q rows bf16
     static constexpr int kOffRow = kOffDS + 2 * kHalfBytes;          // LSE2[2][128], D[2][128]
     static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
-    static constexpr int kSmemRaw = kOffBar + 256 + 1024;
+    // No alignment slack: the dynamic shared window starts 1024-byte aligned
+    // (checked at kernel entry).  At least 120 KB so one CTA runs per SM.
+    static constexpr int kSmemRaw = kOffBar + 256;
     static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;
+    static_assert(kSmemBytes <= 232448, "backward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0;     // S^T, then P^T (bf16); later dQ
     static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16)
@@ -187,8 +190,12 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
     using C = BwdCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(p.ctl.err, kErrBounds);
+        return;
+    }
+    uint8_t *smem = smem_raw;
     uint8_t *sK = smem + C::kOffK;
     uint8_t *sV = smem + C::kOffV;
     uint8_t *sQ = smem + C::kOffQ;
@@ -581,6 +588,8 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
                                             (units * pl->d * 4 + 255) / 256 * 256);
     // 1. D = rowsum(dO * O), dQ accumulator = 0
     {
+        cudaError_t e0 = mark(pl, 2, stream);
+        if (e0 != cudaSuccess) return e0;
         const int64_t threads = units * (pl->d / 8);
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
         if (pl->o_dtype == CA_DTYPE_FP32)
@@ -590,6 +599,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
             ca_bwd_pre_kernel<false><<<blocks, 256, 0, stream>>>(o, static_cast<const __nv_bfloat16 *>(d_o), Dvec,
                                                                  dq_acc, units, pl->d);
         cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = mark(pl, 3, stream);
         if (e != cudaSuccess) return e;
     }
     // 2. main pass
@@ -621,6 +631,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
     cudaError_t e = pl->d == 128 ? launch_main_t<128>(pl, tq, tk, tv, tdo, prm, stream)
                                  : launch_main_t<64>(pl, tq, tk, tv, tdo, prm, stream);
+    if (e == cudaSuccess) e = mark(pl, 4, stream);
     if (e != cudaSuccess) return e;
     // 3. dQ accumulator -> bf16
     {
@@ -629,6 +640,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
         ca_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n8);
         e = cudaGetLastError();
     }
+    if (e == cudaSuccess) e = mark(pl, 5, stream);
     return e;
 }
 

@@ -411,8 +411,10 @@ cudaError_t launch_fwd_t(const ca_plan *pl, const CUtensorMap &tq, const CUtenso
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_fwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
+    if ((e = mark(pl, 0, stream)) != cudaSuccess) return e;
     kern<<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return mark(pl, 1, stream);
 }
 
 }  // namespace

@@ -65,6 +65,7 @@ struct ca_plan {
     int64_t n_fwd = 0, n_bwd = 0;
     int64_t workspace_bytes = 0;
     int64_t wait_limit_ns = 2000000000LL;
+    void *const *timing_events = nullptr;  // optional cudaEvent_t[6], see ca_plan_set_timing_events
     int device = 0, num_sms = 0;
     // device metadata (owned)
     ca::DevTask *d_tasks = nullptr;
@@ -86,6 +87,12 @@ ca_status_t cuda_fail(cudaError_t e, const char *what);
 // a box of (64 elements of dim, box_heads, box_rows) and 128-byte swizzle.
 ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32_t heads, int32_t dim,
                          int32_t box_heads, int32_t box_rows);
+
+// Records the plan's timing event `slot` on stream when timing is enabled.
+inline cudaError_t mark(const ca_plan *p, int slot, cudaStream_t stream) {
+    if (!p->timing_events) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(p->timing_events[slot]), stream);
+}
 
 cudaError_t launch_forward(const ca_plan *p, const void *q, const void *k, const void *v, void *o,
                            float *lse, cudaStream_t stream);

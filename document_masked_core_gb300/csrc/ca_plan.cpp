@@ -392,6 +392,16 @@ ca_status_t ca_plan_set_wait_limit(ca_plan_t *p, int64_t ns) {
     return CA_OK;
 }
 
+ca_status_t ca_plan_set_timing_events(ca_plan_t *p, void *const *events, int32_t n_events) {
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    if (events && n_events < 6) return fail(CA_ERR_INVALID_ARG, "need 6 events");
+    if (events)
+        for (int32_t i = 0; i < 6; ++i)
+            if (!events[i]) return fail(CA_ERR_INVALID_ARG, "NULL event");
+    p->timing_events = events;
+    return CA_OK;
+}
+
 ca_status_t ca_forward(const ca_plan_t *p, const void *q, const void *k, const void *v, void *o, float *lse,
                        void *workspace, void *stream) {
     (void)workspace;

@@ -196,6 +196,17 @@ ca_status_t ca_plan_set_wait_limit(ca_plan_t *plan, int64_t ns);
  */
 ca_status_t ca_watchdog_selftest(const ca_plan_t *plan, int64_t limit_ns, void *stream);
 
+/*
+ * Optional per-launch timing for profiling harnesses: when events is not
+ * NULL, ca_forward records events[0] before and events[1] after its kernel,
+ * and ca_backward records events[2] before its preprocess kernel, events[3]
+ * after it, events[4] after the main kernel and events[5] after the dQ
+ * finalize kernel, all on the call's stream.  events is a host array of
+ * n_events (>= 6) cudaEvent_t handles owned by the caller; pass NULL to stop.
+ * The plan keeps the pointer, not a copy of the array.
+ */
+ca_status_t ca_plan_set_timing_events(ca_plan_t *plan, void *const *events, int32_t n_events);
+
 /* Static description of a status code. */
 const char *ca_status_string(ca_status_t status);
 
