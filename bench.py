@@ -196,7 +196,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = W.llama8b_chunk(seed=0)
-    ws = oracle_sample_workload(w, args.oracle_pairs // 2)
+    ws = oracle_sample_workload(w, args.oracle_pairs // 4)
     oracle.build()
     t_warm, _ = time_oracle(ws, max(1, min(args.warmup, 1)))
     t, flops = time_oracle(ws, args.steps)
@@ -253,6 +253,9 @@ def run_gpu(args, rank, world, local):
 
     # ---- timed region: inputs resident in HBM (Q, dO 512 MiB, K, V 128 MiB each: larger than L2)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for row in ev:  # torch creates the underlying cudaEvent on first record
+        for e in row:
+            e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     clocks.start()
@@ -328,7 +331,7 @@ def run_gpu(args, rank, world, local):
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()
-            wsamp = oracle_sample_workload(w, args.oracle_pairs)
+            wsamp = oracle_sample_workload(w, args.oracle_pairs, kv_groups=2)
             t_cpu, f_cpu = time_oracle(wsamp, 1)
             cpu = {"value": f_cpu / t_cpu / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                    "sample": (f"{wsamp.n_docs} leading documents ({wsamp.total_q} tokens, "
@@ -375,7 +378,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--oracle-pairs", type=int, default=8_000_000,
+    ap.add_argument("--oracle-pairs", type=int, default=30_000_000,
                     help="causal pairs per head of the oracle's sample (bounds its CPU time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
