@@ -29,7 +29,7 @@ CA_DTYPE_FP32 = 1
 # names declared in include/ca.h, in order
 EXPORTS = [
     "ca_plan_create", "ca_plan_dry_run", "ca_plan_info", "ca_plan_task_pairs", "ca_plan_destroy",
-    "ca_forward", "ca_backward", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
+    "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
 ]
 
@@ -89,6 +89,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_forward.argtypes = [vp] * 8
     L.ca_backward.restype = st
     L.ca_backward.argtypes = [vp] * 12
+    L.ca_backward_noalloc.restype = st
+    L.ca_backward_noalloc.argtypes = [vp] * 11
     L.ca_merge.restype = st
     L.ca_merge.argtypes = [i32, vp, vp, i32, i64, i32, i32, vp, i32, vp, vp]
     L.ca_device_status.restype = st
@@ -219,6 +221,13 @@ class Plan:
     def backward(self, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=None):
         _check(load().ca_backward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _stream(stream)))
+
+    def backward_noalloc(self, q, k, v, o, lse, d_o, dq, dk, dv, stream=None):
+        """ca_backward_noalloc: the backward with the library's own 16 MiB
+        scratch array instead of a caller workspace (for callers that cannot
+        allocate device memory; calls on one device must not overlap)."""
+        _check(load().ca_backward_noalloc(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                          _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
     def device_status(self, stream=None) -> int:
         """Sync the stream and return (and clear) the device error status."""

@@ -161,6 +161,30 @@ ca_status_t ca_backward(const ca_plan_t *plan, const void *q, const void *k, con
                         void *dq, void *dk, void *dv, void *workspace, void *stream);
 
 /*
+ * ca_backward without a workspace argument, for callers that cannot allocate
+ * device memory: code inside a host framework that owns every device
+ * allocation (a fixed arena or caching allocator it may not bypass), or
+ * plug-in code handed only its input and output buffers.  The papers have no
+ * counterpart to this entry point; it exists for such callers only.
+ *
+ * The scratch (fp32 dQ accumulator and D vector) lives in one file-scope
+ * device array of 16 MiB that every GPU loading libca.so holds until the
+ * process exits.  Plans whose ca_plan_info().workspace_bytes exceed 16 MiB
+ * are rejected with CA_ERR_UNSUPPORTED before any launch.  The entry point
+ * calls no cudaMalloc, cudaFree or other allocating routine.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * All calls on a device share the array: calls that overlap on the GPU (on
+ * different streams, or from several threads) race and give wrong results,
+ * so serialise them.  The array keeps the last call's contents; every call
+ * clears what must start at zero itself.  Arguments and results are those of
+ * ca_backward.
+ */
+ca_status_t ca_backward_noalloc(const ca_plan_t *plan, const void *q, const void *k, const void *v,
+                                const void *o, const float *lse, const void *d_o,
+                                void *dq, void *dk, void *dv, void *stream);
+
+/*
  * Merge of partial results over KV blocks (million-token paper, Appendix B,
  * Eq. 4): for every (row, head), with M = max_s LSE_s and w_s = exp(LSE_s - M),
  *   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s.
