@@ -216,6 +216,54 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_step):
+    """The same step through the C ABI with host buffers: pinned host -> device
+    copies of Q, K, V, dO and device -> host copies of dQ, dK, dV inside every
+    timed step."""
+    import torch
+    q, k, v, do = inputs
+    o, lse = fwd_out
+    dq, dk, dv = grads
+    sh = stream.cuda_stream
+    hq = q.cpu().pin_memory()
+    hk = k.cpu().pin_memory()
+    hv = v.cpu().pin_memory()
+    hdo = do.cpu().pin_memory()
+    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+    hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
+    hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    q2, k2, v2, do2 = (torch.empty_like(x) for x in (q, k, v, do))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dst, src in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
+                dst.copy_(src, non_blocking=True)
+            plan.forward(q2, k2, v2, o, lse, ws, stream=sh)
+            plan.backward(q2, k2, v2, o, lse, do2, dq_, dk_, dv_, ws, stream=sh)
+            for dst, src in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    stream.synchronize()
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world)
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the end-to-end region")
+
+    return {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local):
@@ -227,7 +275,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     seed = args.seed + rank
-    w = W.llama8b_chunk(seed=seed)
+    w = W.llama8b_chunk(seed=seed, total=args.tokens)
     q, k, v, do = W.make_tensors(w, device=dev)
     stream = torch.cuda.Stream(device=dev)
     t0 = time.perf_counter()
@@ -284,40 +332,9 @@ def run_gpu(args, rank, world, local):
     fin_ms = float(np.mean([e[4].elapsed_time(e[5]) for e in ev]))
 
     # ---- end to end through the C ABI with host buffers
-    hq = q.cpu().pin_memory()
-    hk = k.cpu().pin_memory()
-    hv = v.cpu().pin_memory()
-    hdo = do.cpu().pin_memory()
-    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
-    hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
-    hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
-    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    q2, k2, v2, do2 = (torch.empty_like(x) for x in (q, k, v, do))
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-    d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for dst, src in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
-                dst.copy_(src, non_blocking=True)
-            plan.forward(q2, k2, v2, o, lse, ws, stream=sh)
-            plan.backward(q2, k2, v2, o, lse, do2, dq_, dk_, dv_, ws, stream=sh)
-            for dst, src in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
-                dst.copy_(src, non_blocking=True)
-
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
-    stream.synchronize()
-    barrier(world)
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e2.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world)
-    if plan.device_status(stream=sh) != 0:
-        raise RuntimeError("device error in the end-to-end region")
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, plan, stream, (q, k, v, do), (o, lse), (dq, dk, dv), ws, world, flops_step)
 
     pk, pk_kind = peaks()
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
@@ -361,8 +378,7 @@ def run_gpu(args, rank, world, local):
                          "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": None,
                          "peak_kind": f"bf16 burst, {pk_kind}",
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
-            "e2e": {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "e2e": e2e,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -381,6 +397,9 @@ def main():
     ap.add_argument("--oracle-pairs", type=int, default=30_000_000,
                     help="causal pairs per head of the oracle's sample (bounds its CPU time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--tokens", type=int, default=65536,
+                    help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
