@@ -364,7 +364,8 @@ def run_gpu(args, rank, world, local):
                 "heads": f"{w.num_q_heads}q/{w.num_kv_heads}kv", "head_dim": w.head_dim,
                 "causal_pairs_per_head": info["causal_pairs"], "flops_per_step": flops_step,
                 "flop_count": "12*head_dim*H_q*causal_pairs (4d forward + 8d backward)",
-                "l2": "inputs larger than L2 (Q and dO 512 MiB, K and V 128 MiB each)",
+                "l2": (f"inputs larger than L2 (Q and dO {q.numel() * 2 >> 20} MiB, K and V "
+                       f"{k.numel() * 2 >> 20} MiB each; L2 is 129 MB)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                 "plan_ms": plan_ms,
             },

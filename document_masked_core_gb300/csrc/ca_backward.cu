@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t act = 0, qt = 0;
             bool ok = true;
-            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 if (!(ok = mbar_wait(&bars.kv_empty, (act & 1) ^ 1, wd))) break;
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
                            do_base = smem_u32(sDO), ds_base = smem_u32(sDS);
-            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t lane_addr = (warp * 32u) << 16;
         uint32_t qt = 0;
         bool ok = true;
-        for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
             const KvGeo kg = decode_kv(p, idx);
             const int32_t kpos = kg.jt * kTileKeys + static_cast<int32_t>(i);  // this thread's key
             const bool key_in_doc = kpos < kg.doc_len;

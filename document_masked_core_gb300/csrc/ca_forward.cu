@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, act = 0;
             bool ok = true;
-            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
                 if (!(ok = mbar_wait(&bars.q_empty, (act & 1) ^ 1, wd))) break;
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
                 umma_commit(&bars.s_full[b]);
                 return true;
             };
-            for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
                 if (!(ok = mbar_wait(&bars.q_full, act & 1, wd))) break;
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t lane_addr = (warp * 32u) << 16;
         uint32_t s_it = 0;
         bool ok = true;
-        for (int32_t idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x) {
+        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
             const ItemGeo gi = decode_item(p, idx);
             const int32_t tok = row / p.G;
             const int32_t h = gi.g * p.G + (row % p.G);

@@ -286,7 +286,22 @@ ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64
             p->bwd_tile_pairs += static_cast<int64_t>(nq) * p->hkv;
         }
     }
-    std::stable_sort(bwd.begin(), bwd.end(), [](const BwdItem &a, const BwdItem &b) { return a.n_q > b.n_q; });
+    // Group the items of one (document, kv head): CTAs that run at the same
+    // time then add into the same rows of the fp32 dQ accumulator, which keeps
+    // that working set (document length x G x head_dim x 4 bytes) in L2.
+    // Groups with the most work first; longest items first inside a group.
+    {
+        std::vector<int64_t> group_work(static_cast<size_t>(n_docs) * p->hkv, 0);
+        for (const BwdItem &b : bwd) group_work[static_cast<size_t>(b.doc) * p->hkv + b.g] += b.n_q;
+        std::stable_sort(bwd.begin(), bwd.end(), [&](const BwdItem &a, const BwdItem &b) {
+            const int64_t wa = group_work[static_cast<size_t>(a.doc) * p->hkv + a.g];
+            const int64_t wb = group_work[static_cast<size_t>(b.doc) * p->hkv + b.g];
+            if (wa != wb) return wa > wb;
+            if (a.doc != b.doc) return a.doc < b.doc;
+            if (a.g != b.g) return a.g < b.g;
+            return a.n_q > b.n_q;
+        });
+    }
     p->n_bwd = static_cast<int64_t>(bwd.size());
 
     // workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned
