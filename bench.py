@@ -148,15 +148,21 @@ def max_over_ranks(x: float, world: int) -> float:
 # ----------------------------------------------------------------------------- oracle sample
 
 def oracle_sample_workload(w, pair_budget: int, kv_groups: int = 1):
-    """Bounded sample of the chunk: its leading documents (at least one) whose
-    causal pairs per head stay within pair_budget, each one CA-task, with the
-    first ``kv_groups`` KV heads and their query heads."""
+    """Bounded sample of the chunk: its leading documents whose causal pairs
+    per head stay within pair_budget (or the leading tokens of the first one),
+    each one CA-task, with the first ``kv_groups`` KV heads and their query
+    heads."""
     import workloads as W
     lens = []
     acc = 0
     for L in w.doc_len:
         p = int(L) * (int(L) + 1) // 2
-        if lens and acc + p > pair_budget:
+        if acc + p > pair_budget:
+            if not lens:  # the first document alone is over budget: keep its leading tokens
+                l = int((2 * pair_budget) ** 0.5)
+                while l > 1 and l * (l + 1) // 2 > pair_budget:
+                    l -= 1
+                lens.append(max(1, l))
             break
         lens.append(int(L))
         acc += p
