@@ -1,22 +1,31 @@
 // Forward core attention over a rebatched pool of CA-tasks (sm_103a).
 //
-// One persistent CTA per SM walks the plan's forward tiles (longest first).
-// A tile is 128 query rows = (128 / G tokens) x (G heads of one kv head g), so
-// one K/V tile of 128 keys of head g serves all 128 rows (GQA sharing by
-// packing heads into the MMA M dimension).  For each visible 128-key tile:
-//   S = Q K^T            tcgen05.mma, bf16 x bf16 -> fp32 in TMEM (2 buffers)
-//   online softmax       one thread per row reads its S row from TMEM, masks
-//                        the causal / block edges, keeps the running max m and
-//                        sum l (log2 domain), writes P as bf16 over S in TMEM
-//   O += P V             tcgen05.mma with A = P from TMEM, B = V (MN-major)
+// One persistent CTA per SM walks the plan's forward items (longest first).
+// An item is two consecutive 128-row query tiles A and B of one task and one
+// kv head g; a tile row is one (token, head) pair, 128 / G tokens x G heads,
+// so one 128-key K/V tile of head g serves both tiles (GQA sharing by packing
+// heads into the MMA M dimension).  For each visible key tile j:
+//   S_X = Q_X K_j^T        tcgen05.mma, bf16 x bf16 -> fp32 in TMEM
+//   online softmax         one thread per row reads its S row from TMEM,
+//                          masks the causal / block edges, keeps the running
+//                          max m and sum l (log2 domain), writes P (bf16)
+//                          over S in TMEM
+//   O_X += P_X V_j         tcgen05.mma with A = P from TMEM, B = V (MN-major)
 // and finally O /= l, LSE = ln 2 (m + log2 l).  The online-softmax recurrence
-// with saved row statistics is the one the disaggregation paper relies on
+// with saved row statistics is what the disaggregation paper relies on
 // (Efficient Long-context Language Model Training by Core Attention
 // Disaggregation, §3.4 "Property 1: Statelessness"); fully masked key tiles
 // are never visited (the plan lists only visible tiles).
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue (thread i <-> TMEM
-// lane i <-> tile row i), warp 4 TMA producer, warp 5 TMEM owner + MMA issuer.
+// The two tiles ping-pong on the tensor core: while warpgroup A computes the
+// softmax of S_A(j), the MMA warp runs PV_B(j-1) and S_B(j), and vice versa.
+// The running max is rescaled lazily: a row's O and l are rescaled only when
+// its max grows by more than 2^8, otherwise exponentials are taken against
+// the stale max (values up to 2^8, exact in the final normalisation).
+//
+// Warp roles (320 threads): warps 0-3 softmax + epilogue of tile A, warps 4-7
+// of tile B (thread i of a warpgroup <-> TMEM lane i <-> tile row i), warp 8
+// TMA producer, warp 9 TMEM owner + MMA issuer.
 #include <algorithm>
 #include <cmath>
 
@@ -43,55 +52,72 @@ struct FwdParams {
 template <int D>
 struct FwdCfg {
     static constexpr int kStages = 2;
-    static constexpr int kHalfBytes = 128 * 128;            // 128 rows x 64 bf16
+    static constexpr int kHalfBytes = 128 * 128;              // 128 rows x 64 bf16
     static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffQ = 0;                           // Q_A, Q_B
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    // + barriers + alignment slack; at least 120 KB so that one CTA (which
-    // owns all 512 TMEM columns) runs per SM
-    static constexpr int kSmemBytes = (kOffBar + 512 + 1024) > 122880 ? (kOffBar + 512 + 1024) : 122880;
+    static constexpr int kSmemRaw = kOffBar + 512;
+    static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;  // one CTA per SM
+    static_assert(kSmemBytes <= 232448, "forward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0;    // S/P buffers at 0 and 128
-    static constexpr uint32_t kColO = 256;  // O accumulator, D columns
+    // TMEM columns: S/P of tile X at 128 X, O of tile X at 256 + D X
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = 256;
     static constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
 };
 
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
 struct FwdBars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[2], v_full[2], kv_empty[2];
     uint64_t s_full[2], p_full[2];
-    uint64_t o_full, o_empty, mma_done;
+    uint64_t o_full[2], o_empty[2];
+    uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
 
-struct ItemGeo {
-    int32_t g, row0, p_first, ntok, kv_start, kv_end, kv_off, j_first, n_kv;
+struct TileGeo {
+    int32_t row0, p_first, ntok, n_kv;  // n_kv = 0: tile absent or sees nothing
 };
+
+struct ItemGeo {
+    int32_t g, kv_start, kv_end, kv_off, j_first, n_kv;
+    TileGeo t[2];
+};
+
+__device__ __forceinline__ TileGeo tile_geo(const DevTask &t, int32_t tile, int32_t tpt) {
+    TileGeo tg;
+    const int32_t tok0 = tile * tpt;
+    tg.row0 = t.row0 + tok0;
+    tg.p_first = t.q_start + tok0;
+    tg.ntok = min(tpt, t.q_len - tok0);
+    if (tg.ntok <= 0) {
+        tg.ntok = 0;
+        tg.n_kv = 0;
+        return tg;
+    }
+    const int32_t hi = min(t.kv_start + t.kv_len, tg.p_first + tg.ntok);  // exclusive
+    tg.n_kv = hi <= t.kv_start ? 0 : (hi - 1) / kTileKeys - t.kv_start / kTileKeys + 1;
+    return tg;
+}
 
 __device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) {
     const FwdItem it = p.items[idx];
     const DevTask t = p.tasks[it.task];
     ItemGeo gi;
     gi.g = it.g;
-    const int32_t tok0 = it.tile * p.tpt;
-    gi.row0 = t.row0 + tok0;
-    gi.p_first = t.q_start + tok0;
-    gi.ntok = min(p.tpt, t.q_len - tok0);
     gi.kv_start = t.kv_start;
     gi.kv_end = t.kv_start + t.kv_len;
     gi.kv_off = t.kv_off;
-    const int32_t hi = min(gi.kv_end, gi.p_first + gi.ntok);  // exclusive
-    if (hi <= gi.kv_start) {
-        gi.j_first = 0;
-        gi.n_kv = 0;
-    } else {
-        gi.j_first = gi.kv_start / kTileKeys;
-        gi.n_kv = (hi - 1) / kTileKeys - gi.j_first + 1;
-    }
+    gi.j_first = t.kv_start / kTileKeys;
+    gi.t[0] = tile_geo(t, it.tile, p.tpt);
+    gi.t[1] = tile_geo(t, it.tile + 1, p.tpt);
+    gi.n_kv = max(gi.t[0].n_kv, gi.t[1].n_kv);
     return gi;
 }
 
@@ -109,12 +135,29 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 }
 
 template <int D, bool OUT_F32>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ void store_row_zero(const FwdParams &p, size_t out_idx) {
+    if (OUT_F32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+    p.lse[out_idx] = -INFINITY;
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(320, 1)
     ca_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using C = FwdCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(p.ctl.err, kErrBounds);
+        return;
+    }
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sK = smem + C::kOffK;
     uint8_t *sV = smem + C::kOffV;
@@ -124,28 +167,28 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane = lane_id();
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars.q_full, 1);
-        mbar_init(&bars.q_empty, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars.q_full[x], 1);
+            mbar_init(&bars.q_empty[x], 1);
+            mbar_init(&bars.s_full[x], 1);
+            mbar_init(&bars.p_full[x], 128);
+            mbar_init(&bars.o_full[x], 1);
+            mbar_init(&bars.o_empty[x], 128);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars.s_full[b], 1);
-            mbar_init(&bars.p_full[b], 128);
-        }
-        mbar_init(&bars.o_full, 1);
-        mbar_init(&bars.o_empty, 128);
         mbar_init(&bars.mma_done, 1);
         bars.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&bars.tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -156,20 +199,26 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = bars.tmem_base;
     const Watchdog wd{&p.ctl, &bars.abort_flag};
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t kv_it = 0, act = 0;
+            uint32_t kv_it = 0, q_it[2] = {0, 0};
             bool ok = true;
             for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
-                if (!(ok = mbar_wait(&bars.q_empty, (act & 1) ^ 1, wd))) break;
-                mbar_arrive_expect_tx(&bars.q_full, C::kTileBytes);
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tma_load_3d(sQ + h * C::kHalfBytes, &tm_q, &bars.q_full, h * 64, gi.g * p.G, gi.row0);
-                for (int32_t i = 0; i < gi.n_kv; ++i, ++kv_it) {
+                for (int x = 0; x < 2; ++x) {
+                    if (gi.t[x].n_kv == 0) continue;
+                    if (!(ok = mbar_wait(&bars.q_empty[x], (q_it[x] & 1) ^ 1, wd))) break;
+                    mbar_arrive_expect_tx(&bars.q_full[x], C::kTileBytes);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        tma_load_3d(sQ + x * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[x], h * 64,
+                                    gi.g * p.G, gi.t[x].row0);
+                    ++q_it[x];
+                }
+                for (int32_t i = 0; i < gi.n_kv && ok; ++i, ++kv_it) {
                     const uint32_t st = kv_it % C::kStages;
                     const uint32_t ph = (kv_it / C::kStages) & 1;
                     if (!(ok = mbar_wait(&bars.kv_empty[st], ph ^ 1, wd))) break;
@@ -185,64 +234,75 @@ __global__ void __launch_bounds__(192, 1)
                         tma_load_3d(sV + st * C::kTileBytes + h * C::kHalfBytes, &tm_v, &bars.v_full[st], h * 64,
                                     gi.g, key_row);
                 }
-                ++act;
             }
             if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t kv_it = 0, s_it = 0, act = 0;
+            uint32_t kv_it = 0;
+            uint32_t s_it[2] = {0, 0}, q_it[2] = {0, 0}, o_it[2] = {0, 0};
             bool ok = true;
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-            auto issue_s = [&](uint32_t kv_idx, uint32_t s_idx) -> bool {
-                const uint32_t st = kv_idx % C::kStages;
-                if (!mbar_wait(&bars.k_full[st], (kv_idx / C::kStages) & 1, wd)) return false;
+            // S_x = Q_x K^T into tile x's S columns, for the key tile of ring index kvi
+            auto issue_s = [&](int x, uint32_t kvi) -> bool {
+                const uint32_t st = kvi % C::kStages;
+                if (!mbar_wait(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
                 tc_fence_after();
-                const uint32_t b = s_idx & 1;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                    const uint64_t ad = sdesc_sw128(q_base + off, 16, 1024);
+                    const uint64_t ad = sdesc_sw128(q_base + x * C::kTileBytes + off, 16, 1024);
                     const uint64_t bd = sdesc_sw128(k_base + st * C::kTileBytes + off, 16, 1024);
-                    umma_ss(tmem + C::kColS + b * 128, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss(tmem + C::kColS + x * 128, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars.s_full[b]);
+                umma_commit(&bars.s_full[x]);
                 return true;
             };
             for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
-                if (!(ok = mbar_wait(&bars.q_full, act & 1, wd))) break;
-                tc_fence_after();
-                if (!(ok = issue_s(kv_it, s_it))) break;
+                const int32_t nk[2] = {gi.t[0].n_kv, gi.t[1].n_kv};
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (nk[x] == 0) continue;
+                    if (!(ok = mbar_wait(&bars.q_full[x], q_it[x] & 1, wd))) break;
+                    tc_fence_after();
+                    if (!(ok = issue_s(x, kv_it))) break;
+                }
                 for (int32_t i = 0; i < gi.n_kv && ok; ++i) {
-                    if (i + 1 < gi.n_kv && !(ok = issue_s(kv_it + i + 1, s_it + i + 1))) break;
-                    const uint32_t si = s_it + i;
-                    const uint32_t b = si & 1;
-                    if (!(ok = mbar_wait(&bars.p_full[b], (si >> 1) & 1, wd))) break;
                     const uint32_t kvi = kv_it + i;
                     const uint32_t st = kvi % C::kStages;
                     if (!(ok = mbar_wait(&bars.v_full[st], (kvi / C::kStages) & 1, wd))) break;
-                    if (i == 0 && !(ok = mbar_wait(&bars.o_empty, (act & 1) ^ 1, wd))) break;
-                    tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = sdesc_sw128(v_base + st * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
-                        umma_ts(tmem + C::kColO, tmem + C::kColS + b * 128 + kk * 8, bd, C::kIdescPV,
-                                (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int x = 0; x < 2; ++x) {
+                        if (i >= nk[x]) continue;
+                        if (!(ok = mbar_wait(&bars.p_full[x], s_it[x] & 1, wd))) break;
+                        if (i == 0 && !(ok = mbar_wait(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bd =
+                                sdesc_sw128(v_base + st * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
+                            umma_ts(tmem + C::kColO + x * D, tmem + C::kColS + x * 128 + kk * 8, bd, C::kIdescPV,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        ++s_it[x];
+                        if (i + 1 < nk[x]) {
+                            if (!(ok = issue_s(x, kvi + 1))) break;
+                        } else {
+                            umma_commit(&bars.o_full[x]);   // O_x complete
+                            umma_commit(&bars.q_empty[x]);  // Q_x no longer read
+                            ++q_it[x];
+                            ++o_it[x];
+                        }
                     }
+                    if (!ok) break;
                     umma_commit(&bars.kv_empty[st]);
-                    umma_commit(&bars.o_full);
                 }
-                if (!ok) break;
-                umma_commit(&bars.q_empty);
                 kv_it += gi.n_kv;
-                s_it += gi.n_kv;
-                ++act;
             }
-            // every MMA issued above has completed once this arrives
-            umma_commit(&bars.mma_done);
+            umma_commit(&bars.mma_done);  // arrives once every MMA issued above has completed
             const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
             uint32_t zero = 0;
             const Watchdog wd2{&drain, &zero};
@@ -250,114 +310,107 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax + epilogue
-        const uint32_t row = threadIdx.x;  // 0..127
-        const uint32_t lane_addr = (warp * 32u) << 16;
-        uint32_t s_it = 0;
+        // ------------------------------------------------------------ softmax + epilogue (tile x = warp / 4)
+        const int x = static_cast<int>(warp >> 2);
+        const uint32_t row = threadIdx.x & 127u;
+        const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
+        const uint32_t s_addr = tmem + lane_addr + C::kColS + x * 128;
+        const uint32_t o_addr = tmem + lane_addr + C::kColO + x * D;
+        uint32_t s_it = 0, o_it = 0;
         bool ok = true;
         for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
             const ItemGeo gi = decode_item(p, idx);
+            const TileGeo tg = gi.t[x];
             const int32_t tok = row / p.G;
             const int32_t h = gi.g * p.G + (row % p.G);
-            const bool valid = tok < gi.ntok;
-            const int32_t pos = gi.p_first + min(tok, gi.ntok - 1);
+            const bool valid = tok < tg.ntok;
+            const int32_t pos = tg.p_first + min(tok, max(tg.ntok - 1, 0));
             const int32_t kv_lo = gi.kv_start;
             const int32_t kv_hi = min(gi.kv_end, pos + 1);
-            const size_t out_idx = (static_cast<size_t>(gi.row0 + tok) * p.hq + h);
-            if (gi.n_kv == 0) {
-                if (valid) {
-                    if (OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D);
-#pragma unroll
-                        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D);
-#pragma unroll
-                        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-                    }
-                    p.lse[out_idx] = -INFINITY;
-                }
+            const size_t out_idx = static_cast<size_t>(tg.row0 + tok) * p.hq + h;
+            if (tg.n_kv == 0) {
+                if (valid) store_row_zero<D, OUT_F32>(p, out_idx);
                 continue;
             }
             float m = -INFINITY, l = 0.f;
-            for (int32_t i = 0; i < gi.n_kv; ++i) {
-                const uint32_t si = s_it + i;
-                const uint32_t b = si & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[b], (si >> 1) & 1, wd));
+            for (int32_t i = 0; i < tg.n_kv; ++i, ++s_it) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[x], s_it & 1, wd));
                 if (!ok) break;
                 tc_fence_after();
+                // s_full also implies that PV_x(i-1) has completed (issued before S_x(i))
                 uint32_t sr[4][32];
-                const uint32_t s_addr = tmem + lane_addr + C::kColS + b * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
                 const int32_t key0 = (gi.j_first + i) * kTileKeys;
-                const bool need_mask = key0 < kv_lo || key0 + kTileKeys > kv_hi;
-                float mx = -INFINITY;
+                if (key0 < kv_lo || key0 + kTileKeys > kv_hi) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-                        if (need_mask) {
+                        for (int e = 0; e < 32; ++e) {
                             const int32_t key = key0 + c * 32 + e;
-                            if (key < kv_lo || key >= kv_hi) v = -INFINITY;
+                            if (key < kv_lo || key >= kv_hi) sr[c][e] = __float_as_uint(-INFINITY);
                         }
-                        sr[c][e] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
                 }
-                const float m_new = fmaxf(m, mx);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = ex2(m - m_use);
-                float sum = 0.f;
-                uint32_t pk[2][32];
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2(__uint_as_float(sr[c][e]) - m_use);
-                        const float p1 = ex2(__uint_as_float(sr[c][e + 1]) - m_use);
-                        sum += p0 + p1;
+                        mx0 = fmaxf(mx0, __uint_as_float(sr[c][e]));
+                        mx1 = fmaxf(mx1, __uint_as_float(sr[c][e + 1]));
+                    }
+                const float m_tile = fmaxf(mx0, mx1) * p.scale_log2;  // scale > 0 keeps the order
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m == -INFINITY) {
+                    m = m_tile;  // nothing accumulated yet (l = 0, O = 0 or about to be overwritten)
+                } else if (m_tile > m + kRescaleThreshold) {
+                    alpha = ex2(m - m_tile);
+                    m = m_tile;
+                    rescale = true;
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pk[2][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, -m_use));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, -m_use));
+                        sum0 += p0;
+                        sum1 += p1;
                         pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
                     }
-                }
-                l = l * alpha + sum;
+                l = l * alpha + (sum0 + sum1);
                 tmem_st32(s_addr, pk[0]);
                 tmem_st32(s_addr + 32, pk[1]);
-                if (i > 0) {
-                    // rescale the O accumulated so far once PV_{i-1} has landed
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full, (si - 1) & 1, wd));
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
-                        const uint32_t o_addr = tmem + lane_addr + C::kColO;
+                if (i > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t orr[32];
-                            tmem_ld32(o_addr + c * 32, orr);
-                            tmem_ld_wait();
-                            reg_fence(orr);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_addr + c * 32, orr);
+                        tmem_ld_wait();
+                        reg_fence(orr);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                            tmem_st32(o_addr + c * 32, orr);
-                        }
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(o_addr + c * 32, orr);
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars.p_full[b]);
-                m = m_new;
+                mbar_arrive(&bars.p_full[x]);
             }
             if (!ok) break;
-            // epilogue: O / l and LSE
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full, (s_it + gi.n_kv - 1) & 1, wd));
+            // epilogue: O / l and LSE once the last PV of this tile has landed
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[x], o_it & 1, wd));
             if (!ok) break;
+            ++o_it;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const uint32_t o_addr = tmem + lane_addr + C::kColO;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
@@ -374,29 +427,33 @@ __global__ void __launch_bounds__(192, 1)
                                                  __uint_as_float(orr[4 * e + 2]) * inv_l,
                                                  __uint_as_float(orr[4 * e + 3]) * inv_l);
                     } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32);
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             uint4 w;
-                            w.x = pack_bf16(__uint_as_float(orr[8 * e + 0]) * inv_l, __uint_as_float(orr[8 * e + 1]) * inv_l);
-                            w.y = pack_bf16(__uint_as_float(orr[8 * e + 2]) * inv_l, __uint_as_float(orr[8 * e + 3]) * inv_l);
-                            w.z = pack_bf16(__uint_as_float(orr[8 * e + 4]) * inv_l, __uint_as_float(orr[8 * e + 5]) * inv_l);
-                            w.w = pack_bf16(__uint_as_float(orr[8 * e + 6]) * inv_l, __uint_as_float(orr[8 * e + 7]) * inv_l);
+                            w.x = pack_bf16(__uint_as_float(orr[8 * e + 0]) * inv_l,
+                                            __uint_as_float(orr[8 * e + 1]) * inv_l);
+                            w.y = pack_bf16(__uint_as_float(orr[8 * e + 2]) * inv_l,
+                                            __uint_as_float(orr[8 * e + 3]) * inv_l);
+                            w.z = pack_bf16(__uint_as_float(orr[8 * e + 4]) * inv_l,
+                                            __uint_as_float(orr[8 * e + 5]) * inv_l);
+                            w.w = pack_bf16(__uint_as_float(orr[8 * e + 6]) * inv_l,
+                                            __uint_as_float(orr[8 * e + 7]) * inv_l);
                             dst[e] = w;
                         }
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.o_empty);
+            mbar_arrive(&bars.o_empty[x]);
             if (valid) p.lse[out_idx] = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
-            s_it += gi.n_kv;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -412,7 +469,7 @@ cudaError_t launch_fwd_t(const ca_plan *pl, const CUtensorMap &tq, const CUtenso
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_fwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
     if ((e = mark(pl, 0, stream)) != cudaSuccess) return e;
-    kern<<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    kern<<<grid, 320, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return mark(pl, 1, stream);
 }

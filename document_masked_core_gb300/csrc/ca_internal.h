@@ -29,8 +29,9 @@ struct DevTask {
     int32_t doc_len;
 };
 
-// Forward tile: query tile `tile` (tokens [tile*T, tile*T+T) of the task,
-// T = 128 / G) of kv head g; n_kv = number of visible 128-key tiles.
+// Forward item: query tiles `tile` and `tile + 1` (tile even; tokens
+// [tile*T, tile*T+2T) of the task, T = 128 / G) of kv head g, processed
+// together by one CTA; n_kv = visible 128-key tiles of the later tile.
 struct FwdItem {
     int32_t task, g, tile, n_kv;
 };

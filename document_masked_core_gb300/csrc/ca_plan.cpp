@@ -245,15 +245,18 @@ ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64
     }
     p->total_q = row0;
 
-    // forward tiles: (task, kv head, query tile), longest first
+    // forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1),
+    // longest first; the second tile is absent past the task's last tile.
+    // n_kv = key tiles of the later tile (the earlier tile needs a prefix).
     std::vector<FwdItem> &fwd = hp->fwd;
     for (int32_t t = 0; t < n_tasks; ++t) {
         const DevTask &d = p->h_tasks[t];
         const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
-        for (int32_t tile = 0; tile < ntiles; ++tile) {
-            const int32_t nkv = fwd_tile_nkv(d, tile, p->tpt);
-            for (int32_t g = 0; g < p->hkv; ++g) fwd.push_back({t, g, tile, nkv});
-            p->fwd_tile_pairs += static_cast<int64_t>(nkv) * p->hkv;
+        for (int32_t tile = 0; tile < ntiles; tile += 2) {
+            const int32_t na = fwd_tile_nkv(d, tile, p->tpt);
+            const int32_t nb = tile + 1 < ntiles ? fwd_tile_nkv(d, tile + 1, p->tpt) : 0;
+            for (int32_t g = 0; g < p->hkv; ++g) fwd.push_back({t, g, tile, std::max(na, nb)});
+            p->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
         }
     }
     std::stable_sort(fwd.begin(), fwd.end(), [](const FwdItem &a, const FwdItem &b) { return a.n_kv > b.n_kv; });

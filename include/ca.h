@@ -86,7 +86,7 @@ typedef struct {
     int64_t flops_fwd;        /* 4 * head_dim * num_q_heads * causal_pairs */
     int64_t flops_bwd;        /* 8 * head_dim * num_q_heads * causal_pairs */
     int64_t workspace_bytes;  /* device workspace that ca_forward/ca_backward need */
-    int64_t n_fwd_items;      /* forward tiles (task, kv head, 128-row query tile) */
+    int64_t n_fwd_items;      /* forward items (task, kv head, two 128-row query tiles) */
     int64_t n_bwd_items;      /* backward tiles (document, kv head, 128-key tile) */
     int64_t fwd_tile_pairs;   /* (query tile, key tile) pairs the forward computes */
     int64_t bwd_tile_pairs;   /* (key tile, query tile) pairs the backward computes */
