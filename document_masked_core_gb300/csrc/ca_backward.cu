@@ -18,8 +18,9 @@
 //                     dK  += dS^T Q         A = dS^T (bf16) from TMEM
 //                     dQ   = dS K           A = dS (bf16, MN-major) in smem
 //                   dK/dV accumulate in TMEM across all query tiles and all G
-//                   heads of the group (no atomics); dQ of each pair is added
-//                   to the fp32 accumulator with vector atomics.
+//                   heads of the group (no atomics); dQ of each pair goes from
+//                   TMEM through shared memory into the fp32 accumulator by a
+//                   TMA reduce-add.
 //   3. finalize     fp32 dQ -> bf16.
 #include <algorithm>
 #include <cmath>
@@ -101,7 +102,6 @@ struct BwdParams {
     float scale_log2;  // softmax scale * log2(e)
     const float *lse;  // [total_q, hq]
     const float *Dvec; // [total_q, hq]
-    float *dq_acc;     // [total_q, hq, d]
     __nv_bfloat16 *dk, *dv;
     DevCtl ctl;
 };
@@ -124,20 +124,30 @@ struct BwdCfg {
     static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;
     static_assert(kSmemBytes <= 232448, "backward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0;     // S^T, then P^T (bf16); later dQ
-    static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16)
+    static constexpr uint32_t kColS = 0;     // S^T, then P^T (bf16)
+    static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16), then dQ (fp32, D columns)
     static constexpr uint32_t kColDV = 256;
     static constexpr uint32_t kColDK = 256 + D;
     static constexpr uint32_t kIdescST = idesc_bf16(128, 128, false, false);  // K-major x K-major
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);    // TMEM A x MN-major B
     static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
+    // dQ staging for the TMA reduction: D/32 boxes of 32 fp32 columns x 128
+    // rows (16 KB each, 128-byte swizzle), in the Q stage then the dO stage
+    // of the query tile just finished (the MMAs no longer read them).
+    __device__ static uint32_t stage_box_off(int b, uint32_t st) {
+        return b < D / 64 ? kOffQ + st * kTileBytes + b * kHalfBytes
+                          : kOffDO + st * kTileBytes + (b - D / 64) * kHalfBytes;
+    }
 };
 
 struct BwdBars {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, mma_done;
-    uint64_t row_ready[2];
+    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, stg_full, mma_done;
+    uint64_t row_ready[2][2];  // [warpgroup][tile parity]
+    // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
+    // written by warpgroup 1 land in columns warpgroup 0 reads
+    uint64_t s_loaded, dp_loaded;
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -184,11 +194,19 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// Per query tile t (in the order every role enumerates them):
+//   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO |
+//             [ds_full(t)] dK += dS^T Q, dQ = dS K (into the dP^T columns) |
+//             S^T(t+1) when the item has a next tile (S^T(first) at item start)
+//   gradient: P^T(t) -> p_full | dS^T(t) -> ds_full | dQ(t) -> registers ->
+//             dq_empty -> shared staging -> one TMA reduce-add into the fp32
+//             accumulator; the Q/dO stage is released (q_empty) once the
+//             reduction has read it, at the start of the next tile.
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -201,7 +219,9 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sDO = smem + C::kOffDO;
     uint8_t *sDS = smem + C::kOffDS;
-    float *sLse = reinterpret_cast<float *>(smem + C::kOffRow);  // [2][128] (log2 domain)
+    // row statistics of a query tile, double-buffered by tile parity:
+    // log2(e) LSE - log2(scale) (so exp2(scale log2(e) s - that) = scale P) and -D
+    float *sLse = reinterpret_cast<float *>(smem + C::kOffRow);  // [2][128]
     float *sD = sLse + 256;                                        // [2][128]
     BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::kOffBar);
 
@@ -217,26 +237,30 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.p_full, 128);
-        mbar_init(&bars.ds_full, 128);
+        mbar_init(&bars.p_full, 256);
+        mbar_init(&bars.ds_full, 256);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_empty, 128);
-        mbar_init(&bars.acc_empty, 128);
+        mbar_init(&bars.dq_empty, 256);
+        mbar_init(&bars.acc_empty, 256);
+        mbar_init(&bars.stg_full, 256);
         mbar_init(&bars.mma_done, 1);
-        mbar_init(&bars.row_ready[0], 128);
-        mbar_init(&bars.row_ready[1], 128);
+        for (int w = 0; w < 2; ++w)
+            for (int b = 0; b < 2; ++b) mbar_init(&bars.row_ready[w][b], 128);
+        mbar_init(&bars.s_loaded, 256);
+        mbar_init(&bars.dp_loaded, 256);
         bars.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&bars.tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     tc_fence_before();
     __syncthreads();
@@ -244,7 +268,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = bars.tmem_base;
     const Watchdog wd{&p.ctl, &bars.abort_flag};
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t act = 0, qt = 0;
@@ -282,70 +306,72 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t act = 0, qt = 0;
             bool ok = true;
             const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
                            do_base = smem_u32(sDO), ds_base = smem_u32(sDS);
+            // S^T = K Q^T of the query tile in ring slot qi
+            auto issue_st = [&](uint32_t qi) -> bool {
+                const uint32_t st = qi % C::kQStages;
+                if (!mbar_wait(&bars.q_full[st], (qi / C::kQStages) & 1, wd)) return false;
+                tc_fence_after();
+                const uint32_t qb = q_base + st * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                    umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                            C::kIdescST, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&bars.s_full);
+                return true;
+            };
             for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
-                bool first_tile = true;
-                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
-                    const DevTask t = p.tasks[p.doc_tasks[k]];
-                    int32_t first, count;
-                    task_tiles(t, kg.jt, p.tpt, first, count);
-                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
-                        const uint32_t st = qt % C::kQStages;
-                        if (!(ok = mbar_wait(&bars.q_full[st], (qt / C::kQStages) & 1, wd))) break;
-                        // dQ of the previous tile (aliasing S^T) has been read out
-                        if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
-                        tc_fence_after();
-                        const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
-                        // S^T = K Q^T, dP^T = V dO^T
+                tc_fence_after();
+                if (!(ok = issue_st(qt))) break;
+                for (int32_t j = 0; j < kg.n_q && ok; ++j, ++qt) {
+                    const uint32_t st = qt % C::kQStages;
+                    const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
+                    // dP^T = V dO^T, once dQ of the previous tile has left the dP^T columns
+                    if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
+                    tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                            umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024),
-                                    sdesc_sw128(qb + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&bars.s_full);
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                            umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                                    sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&bars.dp_full);
-                        // dV += P^T dO
-                        if (!(ok = mbar_wait(&bars.p_full, qt & 1, wd))) break;
-                        if (first_tile && !(ok = mbar_wait(&bars.acc_empty, (act & 1) ^ 1, wd))) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                                    sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                    (first_tile && kk == 0) ? 0u : 1u);
-                        // dK += dS^T Q ; dQ = dS K
-                        if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
-                                    sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                    (first_tile && kk == 0) ? 0u : 1u);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            umma_ss(tmem + C::kColS, sdesc_sw128(ds_base + kk * 2048, C::kHalfBytes, 1024),
-                                    sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
-                                    kk > 0 ? 1u : 0u);
-                        umma_commit(&bars.dq_full);
-                        umma_commit(&bars.q_empty[st]);
-                        first_tile = false;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                        umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                                sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
                     }
+                    umma_commit(&bars.dp_full);
+                    // dV += P^T dO
+                    if (!(ok = mbar_wait(&bars.p_full, qt & 1, wd))) break;
+                    if (j == 0 && !(ok = mbar_wait(&bars.acc_empty, (act & 1) ^ 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                                sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                (j == 0 && kk == 0) ? 0u : 1u);
+                    // dK += dS^T Q ; dQ = dS K (into the dP^T columns)
+                    if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                                sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                (j == 0 && kk == 0) ? 0u : 1u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_ss(tmem + C::kColDP, sdesc_sw128(ds_base + kk * 2048, C::kHalfBytes, 1024),
+                                sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
+                                kk > 0 ? 1u : 0u);
+                    umma_commit(&bars.dq_full);
+                    // S^T of the next query tile of this key tile
+                    if (j + 1 < kg.n_q && !(ok = issue_st(qt + 1))) break;
                 }
                 if (!ok) break;
                 umma_commit(&bars.kv_empty);
@@ -359,11 +385,21 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax-gradient warps
-        const uint32_t i = threadIdx.x;  // key row of S^T / dP^T lanes; q row of the dQ lanes
-        const uint32_t lane_addr = (warp * 32u) << 16;
+        // ------------------------------------------------------------ gradient warpgroups
+        // Warpgroup w (warps 4w .. 4w+3) owns query rows / S^T columns
+        // 64w .. 64w+63 of every tile and head_dim columns D/2 w .. of dQ, dK, dV.
+        const int wg = static_cast<int>(warp >> 2);
+        const uint32_t i = threadIdx.x & 127u;  // TMEM lane: key row of S^T, dP^T, dK, dV; q row of dQ
+        const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
+        const int c0 = 64 * wg;
+        const bool flusher = threadIdx.x == 0;  // issues the dQ reductions
+        const float log2_scale = lg2(p.scale);
+        const float inv_scale = 1.f / p.scale;
+        const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
         uint32_t qt = 0;
         bool ok = true;
+        bool flush_pending = false;  // flusher: a dQ reduction still reads a Q/dO stage
+        uint32_t flush_stage = 0;
         for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
             const KvGeo kg = decode_kv(p, idx);
             const int32_t kpos = kg.jt * kTileKeys + static_cast<int32_t>(i);  // this thread's key
@@ -371,10 +407,10 @@ __global__ void __launch_bounds__(192, 1)
             const size_t key_out = (static_cast<size_t>(kg.kv_off) + kpos) * p.hkv + kg.g;
             if (kg.n_q == 0) {
                 if (key_in_doc) {
-                    uint4 *a = reinterpret_cast<uint4 *>(p.dk + key_out * D);
-                    uint4 *b = reinterpret_cast<uint4 *>(p.dv + key_out * D);
+                    uint4 *a = reinterpret_cast<uint4 *>(p.dk + key_out * D + wg * (D / 2));
+                    uint4 *b = reinterpret_cast<uint4 *>(p.dv + key_out * D + wg * (D / 2));
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
+                    for (int c = 0; c < D / 16; ++c) {
                         a[c] = make_uint4(0, 0, 0, 0);
                         b[c] = make_uint4(0, 0, 0, 0);
                     }
@@ -391,143 +427,180 @@ __global__ void __launch_bounds__(192, 1)
                     const int32_t ntok = min(p.tpt, t.q_len - tok0);
                     const int32_t p_first = t.q_start + tok0;
                     const int32_t qrow0 = t.row0 + tok0;
-                    // row statistics of this query tile (double-buffered by tile parity)
+                    const uint32_t st = qt % C::kQStages;
+                    if (flusher && flush_pending) {
+                        // the previous tile's reduction has read its staging: release that stage
+                        bulk_wait_group_read0();
+                        mbar_arrive(&bars.q_empty[flush_stage]);
+                        flush_pending = false;
+                    }
                     float *lse_b = sLse + (qt & 1) * 128;
-                    float *d_b = sD + (qt & 1) * 128;
-                    {
-                        const int32_t tok = i / p.G;
-                        const int32_t h = kg.g * p.G + (i % p.G);
+                    float *nd_b = sD + (qt & 1) * 128;
+                    if (i < 64) {  // this warpgroup's 64 rows
+                        const int32_t r = c0 + static_cast<int32_t>(i);
+                        const int32_t tok = r / p.G;
+                        const int32_t h = kg.g * p.G + (r % p.G);
                         float l2 = INFINITY, dd = 0.f;
                         if (tok < ntok) {
                             const size_t ix = static_cast<size_t>(qrow0 + tok) * p.hq + h;
                             const float l = __ldg(p.lse + ix);
-                            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-                            dd = __ldg(p.Dvec + ix);
+                            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
+                            dd = -__ldg(p.Dvec + ix);
                         }
-                        lse_b[i] = l2;
-                        d_b[i] = dd;
+                        lse_b[r] = l2;
+                        nd_b[r] = dd;
                     }
-                    mbar_arrive(&bars.row_ready[qt & 1]);
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_ready[qt & 1], (qt >> 1) & 1, wd));
+                    mbar_arrive(&bars.row_ready[wg][qt & 1]);
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_ready[wg][qt & 1], (qt >> 1) & 1, wd));
                     if (!ok) break;
                     // visible rows for this key: tile rows r (token r / G) with
                     // r_lo <= r < r_hi, i.e. p >= key position and the token inside the task
                     const int32_t r_hi = ntok * p.G;
                     const int32_t r_lo = key_in_block ? max(kpos - p_first, 0) * p.G : r_hi;
-                    // ---- P^T = exp(scale S^T - LSE), masked
+                    const bool edge = r_lo > c0 || r_hi < c0 + 64;
+                    // ---- P'^T = scale P^T = exp2(scale log2(e) S^T - log2(e) LSE + log2(scale))
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, qt & 1, wd));
                     if (!ok) break;
                     tc_fence_after();
-                    float pt[128];
+                    float pt[64];
                     const uint32_t s_addr = tmem + lane_addr + C::kColS;
                     {
-                        const float4 *l4 = reinterpret_cast<const float4 *>(lse_b);
+                        uint32_t sr[2][32];
+                        tmem_ld32(s_addr + c0, sr[0]);
+                        tmem_ld32(s_addr + c0 + 32, sr[1]);
+                        tmem_ld_wait();
+                        reg_fence(sr[0]);
+                        reg_fence(sr[1]);
+                        mbar_arrive(&bars.s_loaded);
+                        const float2 *l2p = reinterpret_cast<const float2 *>(lse_b + c0);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t sr[32];
-                            tmem_ld32(s_addr + c * 32, sr);
-                            tmem_ld_wait();
-                            reg_fence(sr);
+                        for (int e = 0; e < 64; e += 2) {
+                            const float2 s2 = make_float2(__uint_as_float(sr[e >> 5][e & 31]),
+                                                          __uint_as_float(sr[e >> 5][(e & 31) + 1]));
+                            const float2 nl = l2p[e / 2];
+                            const float2 x = __ffma2_rn(s2, c2, make_float2(-nl.x, -nl.y));
+                            pt[e] = ex2(x.x);
+                            pt[e + 1] = ex2(x.y);
+                        }
+                        if (edge) {
 #pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                const float4 lv = l4[(c * 32 + e) / 4];
-                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int r = c * 32 + e + u;
-                                    const float v = ex2(__uint_as_float(sr[e + u]) * p.scale_log2 - la[u]);
-                                    pt[r] = (r >= r_lo && r < r_hi) ? v : 0.f;
-                                }
+                            for (int e = 0; e < 64; ++e) {
+                                const int r = c0 + e;
+                                if (r < r_lo || r >= r_hi) pt[e] = 0.f;
                             }
                         }
-                    }
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
                         uint32_t pk[32];
 #pragma unroll
-                        for (int w = 0; w < 32; ++w) pk[w] = pack_bf16(pt[64 * m + 2 * w], pt[64 * m + 2 * w + 1]);
-                        tmem_st32(s_addr + 32 * m, pk);
+                        for (int w = 0; w < 32; ++w) pk[w] = pack_bf16(pt[2 * w], pt[2 * w + 1]);
+                        if (!mbar_wait(&bars.s_loaded, qt & 1, wd)) ok = false;
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (ok) tmem_st32(s_addr + 32 * wg, pk);  // q rows 64w.. packed two per column
                     }
+                    if (!ok) break;
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&bars.p_full);
-                    // ---- dS^T = scale P^T (dP^T - D): to TMEM (A of dK += dS^T Q) and to
-                    // shared memory as the MN-major A of dQ = dS K (key row i holds q rows
-                    // 0..63 in half 0 and 64..127 in half 1, 16-byte chunks swizzled by i % 8)
+                    // ---- dS'^T = P'^T (dP^T - D) = scale dS^T: to TMEM (A of dK += dS^T Q) and
+                    // to shared memory half w as the MN-major A of dQ = dS K (key row i
+                    // holds q rows 64w .. 64w+63, 16-byte chunks swizzled by i % 8)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, qt & 1, wd));
                     if (!ok) break;
                     tc_fence_after();
                     {
                         const uint32_t dp_addr = tmem + lane_addr + C::kColDP;
-                        const float4 *d4 = reinterpret_cast<const float4 *>(d_b);
+                        const float2 *nd2 = reinterpret_cast<const float2 *>(nd_b + c0);
+                        uint32_t dr[2][32];
+                        tmem_ld32(dp_addr + c0, dr[0]);
+                        tmem_ld32(dp_addr + c0 + 32, dr[1]);
+                        tmem_ld_wait();
+                        reg_fence(dr[0]);
+                        reg_fence(dr[1]);
+                        mbar_arrive(&bars.dp_loaded);
+                        uint8_t *row = sDS + wg * C::kHalfBytes + i * 128;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // q rows 32c .. 32c+31
-                            uint32_t dr[32];
-                            tmem_ld32(dp_addr + 32 * c, dr);
-                            tmem_ld_wait();
-                            reg_fence(dr);
+                        for (int c = 0; c < 2; ++c) {  // q rows 64w + 32c ..
+                            if (c == 0) {
+                                if (!mbar_wait(&bars.dp_loaded, qt & 1, wd)) ok = false;
+                                ok = __all_sync(0xffffffffu, ok);
+                                if (!ok) break;
+                            }
                             uint32_t pk[16];
 #pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                const int r = 32 * c + e;
-                                const float4 dv4 = d4[r / 4];
-                                pk[e / 2] = pack_bf16(p.scale * pt[r] * (__uint_as_float(dr[e]) - dv4.x),
-                                                      p.scale * pt[r + 1] * (__uint_as_float(dr[e + 1]) - dv4.y));
-                                pk[e / 2 + 1] = pack_bf16(p.scale * pt[r + 2] * (__uint_as_float(dr[e + 2]) - dv4.z),
-                                                          p.scale * pt[r + 3] * (__uint_as_float(dr[e + 3]) - dv4.w));
+                            for (int e = 0; e < 32; e += 2) {
+                                const float2 d2 = make_float2(__uint_as_float(dr[c][e]), __uint_as_float(dr[c][e + 1]));
+                                const float2 x = __fmul2_rn(make_float2(pt[32 * c + e], pt[32 * c + e + 1]),
+                                                            __fadd2_rn(d2, nd2[16 * c + e / 2]));
+                                pk[e / 2] = pack_bf16(x.x, x.y);
                             }
-                            // TMEM: q rows 32c.. packed two per column at column 16c
-                            tmem_st16(dp_addr + 16 * c, pk);
-                            uint8_t *row = sDS + (c >> 1) * C::kHalfBytes + i * 128;
+                            tmem_st16(dp_addr + 32 * wg + 16 * c, pk);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                const int c8 = 4 * (c & 1) + j;  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
+                                const int c8 = 4 * c + j;  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
                                 *reinterpret_cast<uint4 *>(row + ((c8 ^ (i & 7)) * 16)) =
                                     make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                             }
                         }
                         tmem_st_wait();
                     }
+                    if (!ok) break;
                     fence_view_async_shared();
                     tc_fence_before();
                     mbar_arrive(&bars.ds_full);
-                    // ---- dQ (lane i = q row i) -> fp32 accumulator
+                    // ---- dQ (lane i = q row i, columns D/2 w ..): TMEM -> registers,
+                    // release the columns, stage in shared memory, one TMA reduce-add
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, qt & 1, wd));
                     if (!ok) break;
                     tc_fence_after();
                     {
-                        const int32_t tok = i / p.G;
-                        const int32_t h = kg.g * p.G + (i % p.G);
-                        float *dst = p.dq_acc + (static_cast<size_t>(qrow0 + tok) * p.hq + h) * D;
-                        const uint32_t q_addr = tmem + lane_addr + C::kColS;
+                        const bool row_ok = static_cast<int32_t>(i / p.G) < ntok;
+                        uint32_t qr[D / 64][32];
+                        const uint32_t q_addr = tmem + lane_addr + C::kColDP + wg * (D / 2);
 #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t qr[32];
-                            tmem_ld32(q_addr + c * 32, qr);
-                            tmem_ld_wait();
-                            reg_fence(qr);
-                            if (tok < ntok) {
+                        for (int c = 0; c < D / 64; ++c) tmem_ld32(q_addr + c * 32, qr[c]);
+                        tmem_ld_wait();
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    atomicAdd(reinterpret_cast<float4 *>(dst + c * 32 + 4 * e),
-                                              make_float4(__uint_as_float(qr[4 * e]), __uint_as_float(qr[4 * e + 1]),
-                                                          __uint_as_float(qr[4 * e + 2]),
-                                                          __uint_as_float(qr[4 * e + 3])));
+                        for (int c = 0; c < D / 64; ++c) reg_fence(qr[c]);
+                        tc_fence_before();
+                        mbar_arrive(&bars.dq_empty);
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c) {
+                            uint8_t *srow = smem + C::stage_box_off(wg * (D / 64) + c, st) + i * 128;
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 v = row_ok ? make_uint4(qr[c][4 * c8], qr[c][4 * c8 + 1], qr[c][4 * c8 + 2],
+                                                                    qr[c][4 * c8 + 3])
+                                                       : make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4 *>(srow + ((c8 ^ (i & 7)) * 16)) = v;
                             }
                         }
                     }
-                    tc_fence_before();
-                    mbar_arrive(&bars.dq_empty);
+                    fence_view_async_shared();
+                    mbar_arrive(&bars.stg_full);
+                    if (flusher) {
+                        if (!mbar_wait(&bars.stg_full, qt & 1, wd)) {
+                            ok = false;
+                        } else {
+#pragma unroll
+                            for (int b = 0; b < D / 32; ++b)
+                                tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
+                            bulk_commit_group();
+                            flush_pending = true;
+                            flush_stage = st;
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                 }
             }
             if (!ok) break;
-            // ---- epilogue: dK, dV of this key tile (lane i = key i); every MMA of
-            // the item completed before the last dq_full
+            // ---- epilogue: dK, dV of this key tile (lane i = key i, columns D/2 w ..);
+            // every MMA of the item completed before the last dq_full.  The dV
+            // accumulator holds scale dV (it summed P' = scale P).
             {
-                const uint32_t dv_addr = tmem + lane_addr + C::kColDV;
-                const uint32_t dk_addr = tmem + lane_addr + C::kColDK;
+                const uint32_t dv_addr = tmem + lane_addr + C::kColDV + wg * (D / 2);
+                const uint32_t dk_addr = tmem + lane_addr + C::kColDK + wg * (D / 2);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t a[32], b[32];
                     tmem_ld32(dv_addr + c * 32, a);
                     tmem_ld32(dk_addr + c * 32, b);
@@ -535,14 +608,15 @@ __global__ void __launch_bounds__(192, 1)
                     reg_fence(a);
                     reg_fence(b);
                     if (key_in_doc) {
-                        uint4 *va = reinterpret_cast<uint4 *>(p.dv + key_out * D + c * 32);
-                        uint4 *kb = reinterpret_cast<uint4 *>(p.dk + key_out * D + c * 32);
+                        uint4 *va = reinterpret_cast<uint4 *>(p.dv + key_out * D + wg * (D / 2) + c * 32);
+                        uint4 *kb = reinterpret_cast<uint4 *>(p.dk + key_out * D + wg * (D / 2) + c * 32);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            va[e] = make_uint4(pack_bf16(__uint_as_float(a[8 * e]), __uint_as_float(a[8 * e + 1])),
-                                               pack_bf16(__uint_as_float(a[8 * e + 2]), __uint_as_float(a[8 * e + 3])),
-                                               pack_bf16(__uint_as_float(a[8 * e + 4]), __uint_as_float(a[8 * e + 5])),
-                                               pack_bf16(__uint_as_float(a[8 * e + 6]), __uint_as_float(a[8 * e + 7])));
+                            va[e] = make_uint4(
+                                pack_bf16(__uint_as_float(a[8 * e]) * inv_scale, __uint_as_float(a[8 * e + 1]) * inv_scale),
+                                pack_bf16(__uint_as_float(a[8 * e + 2]) * inv_scale, __uint_as_float(a[8 * e + 3]) * inv_scale),
+                                pack_bf16(__uint_as_float(a[8 * e + 4]) * inv_scale, __uint_as_float(a[8 * e + 5]) * inv_scale),
+                                pack_bf16(__uint_as_float(a[8 * e + 6]) * inv_scale, __uint_as_float(a[8 * e + 7]) * inv_scale));
                             kb[e] = make_uint4(pack_bf16(__uint_as_float(b[8 * e]), __uint_as_float(b[8 * e + 1])),
                                                pack_bf16(__uint_as_float(b[8 * e + 2]), __uint_as_float(b[8 * e + 3])),
                                                pack_bf16(__uint_as_float(b[8 * e + 4]), __uint_as_float(b[8 * e + 5])),
@@ -554,11 +628,13 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_arrive(&bars.acc_empty);
             }
         }
+        // every dQ reduction has completed before the CTA exits
+        if (flusher) bulk_wait_group0();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -566,14 +642,15 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int D>
 cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const CUtensorMap &tdo, const BwdParams &prm, cudaStream_t stream) {
+                          const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &prm,
+                          cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = ca_bwd_main_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_bwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+    kern<<<grid, 320, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
     return cudaGetLastError();
 }
 
@@ -603,8 +680,9 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
         if (e != cudaSuccess) return e;
     }
     // 2. main pass
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
+        make_tmap_3d(&tdq, dq_acc, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt, true) != CA_OK ||
         make_tmap_3d(&tdo, d_o, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
         make_tmap_3d(&tk, k, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK ||
         make_tmap_3d(&tv, v, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK)
@@ -624,13 +702,12 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     prm.scale_log2 = pl->scale * 1.4426950408889634f;
     prm.lse = lse;
     prm.Dvec = Dvec;
-    prm.dq_acc = dq_acc;
     prm.dk = static_cast<__nv_bfloat16 *>(dk);
     prm.dv = static_cast<__nv_bfloat16 *>(dv);
     prm.ctl.err = pl->d_err;
     prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
-    cudaError_t e = pl->d == 128 ? launch_main_t<128>(pl, tq, tk, tv, tdo, prm, stream)
-                                 : launch_main_t<64>(pl, tq, tk, tv, tdo, prm, stream);
+    cudaError_t e = pl->d == 128 ? launch_main_t<128>(pl, tq, tk, tv, tdo, tdq, prm, stream)
+                                 : launch_main_t<64>(pl, tq, tk, tv, tdo, tdq, prm, stream);
     if (e == cudaSuccess) e = mark(pl, 4, stream);
     if (e != cudaSuccess) return e;
     // 3. dQ accumulator -> bf16

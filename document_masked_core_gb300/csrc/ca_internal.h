@@ -84,10 +84,11 @@ void set_error(const std::string &msg);
 ca_status_t fail(ca_status_t st, const std::string &msg);
 ca_status_t cuda_fail(cudaError_t e, const char *what);
 
-// Builds a 3D bf16 tensor map over a [rows, heads, dim] token-major tensor with
-// a box of (64 elements of dim, box_heads, box_rows) and 128-byte swizzle.
+// Builds a 3D tensor map over a [rows, heads, dim] token-major bf16 (or fp32)
+// tensor with a box of (128 bytes of dim, box_heads, box_rows) and 128-byte
+// swizzle.
 ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32_t heads, int32_t dim,
-                         int32_t box_heads, int32_t box_rows);
+                         int32_t box_heads, int32_t box_rows, bool fp32 = false);
 
 // Records the plan's timing event `slot` on stream when timing is enabled.
 inline cudaError_t mark(const ca_plan *p, int slot, cudaStream_t stream) {

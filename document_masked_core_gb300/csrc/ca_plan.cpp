@@ -81,7 +81,7 @@ ca_status_t cuda_fail(cudaError_t e, const char *what) {
 }
 
 ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32_t heads, int32_t dim,
-                         int32_t box_heads, int32_t box_rows) {
+                         int32_t box_heads, int32_t box_rows, bool fp32) {
     std::call_once(g_encode_once, [] {
         cudaDriverEntryPointQueryResult q{};
         void *fn = nullptr;
@@ -93,10 +93,13 @@ ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32
     if (!g_encode) return fail(CA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     cuuint64_t gdim[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
                           static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
-    cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(heads) * dim * 2};
-    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t esz = fp32 ? 4 : 2;
+    cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * esz, static_cast<cuuint64_t>(heads) * dim * esz};
+    // the box's inner extent is one 128-byte swizzle row: 64 bf16 or 32 fp32
+    cuuint32_t box[3] = {fp32 ? 32u : 64u, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
+    CUresult r = g_encode(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void *>(base), gdim, gstride, box,
                           estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(CA_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(r) + ")");
