@@ -132,11 +132,11 @@ struct BwdCfg {
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);    // TMEM A x MN-major B
     static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
     // dQ staging for the TMA reduction: D/32 boxes of 32 fp32 columns x 128
-    // rows (16 KB each, 128-byte swizzle), in the Q stage then the dO stage
-    // of the query tile just finished (the MMAs no longer read them).
+    // rows (16 KB each, 128-byte swizzle).  Columns 0 .. D/2-1 (warpgroup 0)
+    // go to the dS buffer, columns D/2 .. D-1 (warpgroup 1) to the Q stage of
+    // the query tile just finished; the MMAs no longer read either.
     __device__ static uint32_t stage_box_off(int b, uint32_t st) {
-        return b < D / 64 ? kOffQ + st * kTileBytes + b * kHalfBytes
-                          : kOffDO + st * kTileBytes + (b - D / 64) * kHalfBytes;
+        return b < D / 64 ? kOffDS + b * kHalfBytes : kOffQ + st * kTileBytes + (b - D / 64) * kHalfBytes;
     }
 };
 
@@ -144,10 +144,11 @@ struct BwdBars {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, stg_full, mma_done;
-    uint64_t row_ready[2][2];  // [warpgroup][tile parity]
+    uint64_t row_full[2];      // row statistics of the query tile in Q/dO stage s are in shared memory
     // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
     // written by warpgroup 1 land in columns warpgroup 0 reads
     uint64_t s_loaded, dp_loaded;
+    uint64_t ds_free;  // the dQ reduction has read the dS buffer (dQ staging of warpgroup 0)
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -194,16 +195,20 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// Warp roles (352 threads): warps 0-7 gradient warpgroups, warp 8 producer,
+// warp 9 TMEM owner + MMA issuer, warp 10 dQ flush.
 // Per query tile t (in the order every role enumerates them):
 //   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO |
 //             [ds_full(t)] dK += dS^T Q, dQ = dS K (into the dP^T columns) |
 //             S^T(t+1) when the item has a next tile (S^T(first) at item start)
 //   gradient: P^T(t) -> p_full | dS^T(t) -> ds_full | dQ(t) -> registers ->
-//             dq_empty -> shared staging -> one TMA reduce-add into the fp32
-//             accumulator; the Q/dO stage is released (q_empty) once the
-//             reduction has read it, at the start of the next tile.
+//             dq_empty -> shared staging (dS buffer and the Q stage of tile t)
+//             -> stg_full
+//   flush:    TMA reduce-adds of the staging into the fp32 accumulator; the
+//             Q/dO stage is released (q_empty) once its half has been read,
+//             the dS buffer (ds_free) once the other half has.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -219,8 +224,9 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sDO = smem + C::kOffDO;
     uint8_t *sDS = smem + C::kOffDS;
-    // row statistics of a query tile, double-buffered by tile parity:
-    // log2(e) LSE - log2(scale) (so exp2(scale log2(e) s - that) = scale P) and -D
+    // row statistics of the query tile in each Q/dO stage, written by the
+    // producer warp: log2(e) LSE - log2(scale) (so exp2(scale log2(e) s - that)
+    // = scale P) and -D
     float *sLse = reinterpret_cast<float *>(smem + C::kOffRow);  // [2][128]
     float *sD = sLse + 256;                                        // [2][128]
     BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::kOffBar);
@@ -244,10 +250,10 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(&bars.acc_empty, 256);
         mbar_init(&bars.stg_full, 256);
         mbar_init(&bars.mma_done, 1);
-        for (int w = 0; w < 2; ++w)
-            for (int b = 0; b < 2; ++b) mbar_init(&bars.row_ready[w][b], 128);
+        for (int b = 0; b < 2; ++b) mbar_init(&bars.row_full[b], 32);
         mbar_init(&bars.s_loaded, 256);
         mbar_init(&bars.dp_loaded, 256);
+        mbar_init(&bars.ds_free, 1);
         bars.abort_flag = 0;
         fence_mbar_init();
     }
@@ -270,41 +276,70 @@ __global__ void __launch_bounds__(320, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // Lane 0 issues the TMA loads; all 32 lanes fill the row statistics of
+        // each query tile (LSE, D from global memory) ahead of their use.
+        {
             uint32_t act = 0, qt = 0;
             bool ok = true;
+            const float log2_scale = lg2(p.scale);
             for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
-                if (!(ok = mbar_wait(&bars.kv_empty, (act & 1) ^ 1, wd))) break;
-                const int32_t key_row = kg.kv_off + kg.jt * kTileKeys;
-                mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
+                if (lane == 0) {
+                    ok = mbar_wait(&bars.kv_empty, (act & 1) ^ 1, wd);
+                    if (ok) {
+                        const int32_t key_row = kg.kv_off + kg.jt * kTileKeys;
+                        mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    tma_load_3d(sK + h * C::kHalfBytes, &tm_k, &bars.kv_full, h * 64, kg.g, key_row);
-                    tma_load_3d(sV + h * C::kHalfBytes, &tm_v, &bars.kv_full, h * 64, kg.g, key_row);
+                        for (int h = 0; h < D / 64; ++h) {
+                            tma_load_3d(sK + h * C::kHalfBytes, &tm_k, &bars.kv_full, h * 64, kg.g, key_row);
+                            tma_load_3d(sV + h * C::kHalfBytes, &tm_v, &bars.kv_full, h * 64, kg.g, key_row);
+                        }
+                    }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
                 for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
                     const DevTask t = p.tasks[p.doc_tasks[k]];
                     int32_t first, count;
                     task_tiles(t, kg.jt, p.tpt, first, count);
                     for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
                         const uint32_t st = qt % C::kQStages;
-                        if (!(ok = mbar_wait(&bars.q_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd))) break;
-                        const int32_t qrow = t.row0 + tile * p.tpt;
-                        mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kTileBytes);
+                        if (lane == 0) ok = mbar_wait(&bars.q_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
+                        const int32_t tok0 = tile * p.tpt;
+                        const int32_t qrow = t.row0 + tok0;
+                        const int32_t ntok = min(p.tpt, t.q_len - tok0);
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kTileBytes);
 #pragma unroll
-                        for (int h = 0; h < D / 64; ++h) {
-                            tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
-                                        h * 64, kg.g * p.G, qrow);
-                            tma_load_3d(sDO + st * C::kTileBytes + h * C::kHalfBytes, &tm_do, &bars.q_full[st],
-                                        h * 64, kg.g * p.G, qrow);
+                            for (int h = 0; h < D / 64; ++h) {
+                                tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
+                                            h * 64, kg.g * p.G, qrow);
+                                tma_load_3d(sDO + st * C::kTileBytes + h * C::kHalfBytes, &tm_do, &bars.q_full[st],
+                                            h * 64, kg.g * p.G, qrow);
+                            }
                         }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int32_t r = static_cast<int32_t>(lane) + 32 * j;
+                            const int32_t tok = r / p.G;
+                            float l2 = INFINITY, nd = 0.f;
+                            if (tok < ntok) {
+                                const size_t ix = static_cast<size_t>(qrow + tok) * p.hq + kg.g * p.G + (r % p.G);
+                                const float l = __ldg(p.lse + ix);
+                                l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
+                                nd = -__ldg(p.Dvec + ix);
+                            }
+                            sLse[st * 128 + r] = l2;
+                            sD[st * 128 + r] = nd;
+                        }
+                        mbar_arrive(&bars.row_full[st]);
                     }
                 }
                 ++act;
             }
-            if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
+            if (!ok && lane == 0) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
@@ -384,6 +419,45 @@ __global__ void __launch_bounds__(320, 1)
             mbar_wait(&bars.mma_done, 0, wd2);
         }
         __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ dQ flush
+        // Lane 0: once both gradient warpgroups have staged dQ of a query tile
+        // in its Q/dO stage, add it into the fp32 accumulator with TMA
+        // reduce-adds, wait until they have read the staging and release the
+        // stage to the producer.
+        if (lane == 0) {
+            uint32_t qt = 0;
+            bool ok = true;
+            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+                const KvGeo kg = decode_kv(p, idx);
+                if (kg.n_q == 0) continue;
+                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                    const DevTask t = p.tasks[p.doc_tasks[k]];
+                    int32_t first, count;
+                    task_tiles(t, kg.jt, p.tpt, first, count);
+                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                        const uint32_t st = qt % C::kQStages;
+                        if (!(ok = mbar_wait(&bars.stg_full, qt & 1, wd))) break;
+                        const int32_t qrow0 = t.row0 + tile * p.tpt;
+                        // the half staged in the Q stage first: releasing the stage early keeps
+                        // the producer ahead; then the half staged in the dS buffer
+#pragma unroll
+                        for (int b = D / 64; b < D / 32; ++b)
+                            tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
+                        bulk_commit_group();
+#pragma unroll
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
+                        bulk_commit_group();
+                        bulk_wait_group_read1();
+                        mbar_arrive(&bars.q_empty[st]);
+                        bulk_wait_group_read0();
+                        mbar_arrive(&bars.ds_free);
+                    }
+                }
+            }
+            bulk_wait_group0();  // every dQ reduction has completed before the CTA exits
+        }
     } else {
         // ------------------------------------------------------------ gradient warpgroups
         // Warpgroup w (warps 4w .. 4w+3) owns query rows / S^T columns
@@ -392,14 +466,10 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t i = threadIdx.x & 127u;  // TMEM lane: key row of S^T, dP^T, dK, dV; q row of dQ
         const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
         const int c0 = 64 * wg;
-        const bool flusher = threadIdx.x == 0;  // issues the dQ reductions
-        const float log2_scale = lg2(p.scale);
         const float inv_scale = 1.f / p.scale;
         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
         uint32_t qt = 0;
         bool ok = true;
-        bool flush_pending = false;  // flusher: a dQ reduction still reads a Q/dO stage
-        uint32_t flush_stage = 0;
         for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
             const KvGeo kg = decode_kv(p, idx);
             const int32_t kpos = kg.jt * kTileKeys + static_cast<int32_t>(i);  // this thread's key
@@ -428,30 +498,9 @@ __global__ void __launch_bounds__(320, 1)
                     const int32_t p_first = t.q_start + tok0;
                     const int32_t qrow0 = t.row0 + tok0;
                     const uint32_t st = qt % C::kQStages;
-                    if (flusher && flush_pending) {
-                        // the previous tile's reduction has read its staging: release that stage
-                        bulk_wait_group_read0();
-                        mbar_arrive(&bars.q_empty[flush_stage]);
-                        flush_pending = false;
-                    }
-                    float *lse_b = sLse + (qt & 1) * 128;
-                    float *nd_b = sD + (qt & 1) * 128;
-                    if (i < 64) {  // this warpgroup's 64 rows
-                        const int32_t r = c0 + static_cast<int32_t>(i);
-                        const int32_t tok = r / p.G;
-                        const int32_t h = kg.g * p.G + (r % p.G);
-                        float l2 = INFINITY, dd = 0.f;
-                        if (tok < ntok) {
-                            const size_t ix = static_cast<size_t>(qrow0 + tok) * p.hq + h;
-                            const float l = __ldg(p.lse + ix);
-                            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
-                            dd = -__ldg(p.Dvec + ix);
-                        }
-                        lse_b[r] = l2;
-                        nd_b[r] = dd;
-                    }
-                    mbar_arrive(&bars.row_ready[wg][qt & 1]);
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_ready[wg][qt & 1], (qt >> 1) & 1, wd));
+                    const float *lse_b = sLse + st * 128;
+                    const float *nd_b = sD + st * 128;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_full[st], (qt / C::kQStages) & 1, wd));
                     if (!ok) break;
                     // visible rows for this key: tile rows r (token r / G) with
                     // r_lo <= r < r_hi, i.e. p >= key position and the token inside the task
@@ -504,6 +553,9 @@ __global__ void __launch_bounds__(320, 1)
                     // to shared memory half w as the MN-major A of dQ = dS K (key row i
                     // holds q rows 64w .. 64w+63, 16-byte chunks swizzled by i % 8)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, qt & 1, wd));
+                    if (!ok) break;
+                    // the dS buffer held dQ staging of the previous tile until its reduction read it
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_free, (qt & 1) ^ 1, wd));
                     if (!ok) break;
                     tc_fence_after();
                     {
@@ -576,20 +628,6 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     fence_view_async_shared();
                     mbar_arrive(&bars.stg_full);
-                    if (flusher) {
-                        if (!mbar_wait(&bars.stg_full, qt & 1, wd)) {
-                            ok = false;
-                        } else {
-#pragma unroll
-                            for (int b = 0; b < D / 32; ++b)
-                                tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
-                            bulk_commit_group();
-                            flush_pending = true;
-                            flush_stage = st;
-                        }
-                    }
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
                 }
             }
             if (!ok) break;
@@ -628,8 +666,6 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_arrive(&bars.acc_empty);
             }
         }
-        // every dQ reduction has completed before the CTA exits
-        if (flusher) bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -650,7 +686,7 @@ cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtens
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_bwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, 320, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
+    kern<<<grid, 352, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
     return cudaGetLastError();
 }
 
