@@ -133,22 +133,24 @@ struct BwdCfg {
     static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
     // dQ staging for the TMA reduction: D/32 boxes of 32 fp32 columns x 128
     // rows (16 KB each, 128-byte swizzle).  Columns 0 .. D/2-1 (warpgroup 0)
-    // go to the dS buffer, columns D/2 .. D-1 (warpgroup 1) to the Q stage of
-    // the query tile just finished; the MMAs no longer read either.
+    // go to the Q tile, columns D/2 .. D-1 (warpgroup 1) to the dO tile of
+    // the query tile just finished (the MMAs no longer read either); the two
+    // regions are released to the producer separately.
     __device__ static uint32_t stage_box_off(int b, uint32_t st) {
-        return b < D / 64 ? kOffDS + b * kHalfBytes : kOffQ + st * kTileBytes + (b - D / 64) * kHalfBytes;
+        return b < D / 64 ? kOffQ + st * kTileBytes + b * kHalfBytes
+                          : kOffDO + st * kTileBytes + (b - D / 64) * kHalfBytes;
     }
 };
 
 struct BwdBars {
     uint64_t kv_full, kv_empty;
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[2], q_empty[2];    // Q tile (and its row statistics) of stage s
+    uint64_t do_full[2], do_empty[2];  // dO tile of stage s
     uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, stg_full, mma_done;
     uint64_t row_full[2];      // row statistics of the query tile in Q/dO stage s are in shared memory
     // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
     // written by warpgroup 1 land in columns warpgroup 0 reads
     uint64_t s_loaded, dp_loaded;
-    uint64_t ds_free;  // the dQ reduction has read the dS buffer (dQ staging of warpgroup 0)
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -202,11 +204,11 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 //             [ds_full(t)] dK += dS^T Q, dQ = dS K (into the dP^T columns) |
 //             S^T(t+1) when the item has a next tile (S^T(first) at item start)
 //   gradient: P^T(t) -> p_full | dS^T(t) -> ds_full | dQ(t) -> registers ->
-//             dq_empty -> shared staging (dS buffer and the Q stage of tile t)
-//             -> stg_full
+//             dq_empty -> shared staging (the Q and dO tiles of tile t) ->
+//             stg_full
 //   flush:    TMA reduce-adds of the staging into the fp32 accumulator; the
-//             Q/dO stage is released (q_empty) once its half has been read,
-//             the dS buffer (ds_free) once the other half has.
+//             Q tile is released (q_empty) once its half has been read, the
+//             dO tile (do_empty) once the other half has.
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -240,6 +242,8 @@ __global__ void __launch_bounds__(352, 1)
         for (int s = 0; s < C::kQStages; ++s) {
             mbar_init(&bars.q_full[s], 1);
             mbar_init(&bars.q_empty[s], 1);
+            mbar_init(&bars.do_full[s], 1);
+            mbar_init(&bars.do_empty[s], 1);
         }
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
@@ -253,7 +257,6 @@ __global__ void __launch_bounds__(352, 1)
         for (int b = 0; b < 2; ++b) mbar_init(&bars.row_full[b], 32);
         mbar_init(&bars.s_loaded, 256);
         mbar_init(&bars.dp_loaded, 256);
-        mbar_init(&bars.ds_free, 1);
         bars.abort_flag = 0;
         fence_mbar_init();
     }
@@ -311,14 +314,11 @@ __global__ void __launch_bounds__(352, 1)
                         const int32_t qrow = t.row0 + tok0;
                         const int32_t ntok = min(p.tpt, t.q_len - tok0);
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kTileBytes);
+                            mbar_arrive_expect_tx(&bars.q_full[st], C::kTileBytes);
 #pragma unroll
-                            for (int h = 0; h < D / 64; ++h) {
+                            for (int h = 0; h < D / 64; ++h)
                                 tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
                                             h * 64, kg.g * p.G, qrow);
-                                tma_load_3d(sDO + st * C::kTileBytes + h * C::kHalfBytes, &tm_do, &bars.q_full[st],
-                                            h * 64, kg.g * p.G, qrow);
-                            }
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -335,6 +335,18 @@ __global__ void __launch_bounds__(352, 1)
                             sD[st * 128 + r] = nd;
                         }
                         mbar_arrive(&bars.row_full[st]);
+                        if (lane == 0) {
+                            ok = mbar_wait(&bars.do_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
+                            if (ok) {
+                                mbar_arrive_expect_tx(&bars.do_full[st], C::kTileBytes);
+#pragma unroll
+                                for (int h = 0; h < D / 64; ++h)
+                                    tma_load_3d(sDO + st * C::kTileBytes + h * C::kHalfBytes, &tm_do,
+                                                &bars.do_full[st], h * 64, kg.g * p.G, qrow);
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
                     }
                 }
                 ++act;
@@ -373,6 +385,7 @@ __global__ void __launch_bounds__(352, 1)
                     const uint32_t st = qt % C::kQStages;
                     const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
                     // dP^T = V dO^T, once dQ of the previous tile has left the dP^T columns
+                    if (!(ok = mbar_wait(&bars.do_full[st], (qt / C::kQStages) & 1, wd))) break;
                     if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
                     tc_fence_after();
 #pragma unroll
@@ -439,20 +452,20 @@ __global__ void __launch_bounds__(352, 1)
                         const uint32_t st = qt % C::kQStages;
                         if (!(ok = mbar_wait(&bars.stg_full, qt & 1, wd))) break;
                         const int32_t qrow0 = t.row0 + tile * p.tpt;
-                        // the half staged in the Q stage first: releasing the stage early keeps
-                        // the producer ahead; then the half staged in the dS buffer
+                        // the half staged in the Q tile first (the next Q load is needed
+                        // sooner, by S^T), then the half staged in the dO tile
 #pragma unroll
-                        for (int b = D / 64; b < D / 32; ++b)
+                        for (int b = 0; b < D / 64; ++b)
                             tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
                         bulk_commit_group();
 #pragma unroll
-                        for (int b = 0; b < D / 64; ++b)
+                        for (int b = D / 64; b < D / 32; ++b)
                             tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
                         bulk_commit_group();
                         bulk_wait_group_read1();
                         mbar_arrive(&bars.q_empty[st]);
                         bulk_wait_group_read0();
-                        mbar_arrive(&bars.ds_free);
+                        mbar_arrive(&bars.do_empty[st]);
                     }
                 }
             }
@@ -553,9 +566,6 @@ __global__ void __launch_bounds__(352, 1)
                     // to shared memory half w as the MN-major A of dQ = dS K (key row i
                     // holds q rows 64w .. 64w+63, 16-byte chunks swizzled by i % 8)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, qt & 1, wd));
-                    if (!ok) break;
-                    // the dS buffer held dQ staging of the previous tile until its reduction read it
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_free, (qt & 1) ^ 1, wd));
                     if (!ok) break;
                     tc_fence_after();
                     {
