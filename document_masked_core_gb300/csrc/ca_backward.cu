@@ -147,7 +147,8 @@ struct BwdBars {
     uint64_t q_full[2], q_empty[2];    // Q tile (and its row statistics) of stage s
     uint64_t do_full[2], do_empty[2];  // dO tile of stage s
     uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, stg_full, mma_done;
-    uint64_t row_full[2];      // row statistics of the query tile in Q/dO stage s are in shared memory
+    uint64_t row_full[2];      // row statistics of query tile t (buffer t % 2) are in shared memory
+    uint64_t row_empty[2];     // the gradient warpgroups are done with buffer t % 2
     // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
     // written by warpgroup 1 land in columns warpgroup 0 reads
     uint64_t s_loaded, dp_loaded;
@@ -197,8 +198,9 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// Warp roles (352 threads): warps 0-7 gradient warpgroups, warp 8 producer,
-// warp 9 TMEM owner + MMA issuer, warp 10 dQ flush.
+// Warp roles (384 threads): warps 0-7 gradient warpgroups, warp 8 TMA
+// producer, warp 9 TMEM owner + MMA issuer, warp 10 dQ flush, warp 11 row
+// statistics (LSE, D) of each query tile.
 // Per query tile t (in the order every role enumerates them):
 //   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO |
 //             [ds_full(t)] dK += dS^T Q, dQ = dS K (into the dP^T columns) |
@@ -210,7 +212,7 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 //             Q tile is released (q_empty) once its half has been read, the
 //             dO tile (do_empty) once the other half has.
 template <int D>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -254,7 +256,10 @@ __global__ void __launch_bounds__(352, 1)
         mbar_init(&bars.acc_empty, 256);
         mbar_init(&bars.stg_full, 256);
         mbar_init(&bars.mma_done, 1);
-        for (int b = 0; b < 2; ++b) mbar_init(&bars.row_full[b], 32);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.row_full[b], 32);
+            mbar_init(&bars.row_empty[b], 256);
+        }
         mbar_init(&bars.s_loaded, 256);
         mbar_init(&bars.dp_loaded, 256);
         bars.abort_flag = 0;
@@ -278,13 +283,10 @@ __global__ void __launch_bounds__(352, 1)
     const Watchdog wd{&p.ctl, &bars.abort_flag};
 
     if (warp == 8) {
-        // ------------------------------------------------------------ producer
-        // Lane 0 issues the TMA loads; all 32 lanes fill the row statistics of
-        // each query tile (LSE, D from global memory) ahead of their use.
+        // ------------------------------------------------------------ producer (lane 0 issues)
         {
             uint32_t act = 0, qt = 0;
             bool ok = true;
-            const float log2_scale = lg2(p.scale);
             for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
@@ -320,21 +322,6 @@ __global__ void __launch_bounds__(352, 1)
                                 tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
                                             h * 64, kg.g * p.G, qrow);
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int32_t r = static_cast<int32_t>(lane) + 32 * j;
-                            const int32_t tok = r / p.G;
-                            float l2 = INFINITY, nd = 0.f;
-                            if (tok < ntok) {
-                                const size_t ix = static_cast<size_t>(qrow + tok) * p.hq + kg.g * p.G + (r % p.G);
-                                const float l = __ldg(p.lse + ix);
-                                l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
-                                nd = -__ldg(p.Dvec + ix);
-                            }
-                            sLse[st * 128 + r] = l2;
-                            sD[st * 128 + r] = nd;
-                        }
-                        mbar_arrive(&bars.row_full[st]);
                         if (lane == 0) {
                             ok = mbar_wait(&bars.do_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
                             if (ok) {
@@ -432,6 +419,50 @@ __global__ void __launch_bounds__(352, 1)
             mbar_wait(&bars.mma_done, 0, wd2);
         }
         __syncwarp();
+    } else if (warp == 11) {
+        // ------------------------------------------------------------ row statistics
+        // All 32 lanes load LSE and D of each query tile's 128 rows from global
+        // memory into a 2-entry buffer ring, ahead of the gradient warpgroups.
+        uint32_t qt = 0;
+        bool ok = true;
+        const float log2_scale = lg2(p.scale);
+        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            const KvGeo kg = decode_kv(p, idx);
+            if (kg.n_q == 0) continue;
+            for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                const DevTask t = p.tasks[p.doc_tasks[k]];
+                int32_t first, count;
+                task_tiles(t, kg.jt, p.tpt, first, count);
+                for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                    const uint32_t b = qt & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_empty[b], ((qt >> 1) & 1) ^ 1, wd));
+                    if (!ok) break;
+                    const int32_t tok0 = tile * p.tpt;
+                    const int32_t qrow = t.row0 + tok0;
+                    const int32_t ntok = min(p.tpt, t.q_len - tok0);
+                    float l2[4], nd[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int32_t r = static_cast<int32_t>(lane) + 32 * j;
+                        const int32_t tok = r / p.G;
+                        l2[j] = INFINITY;
+                        nd[j] = 0.f;
+                        if (tok < ntok) {
+                            const size_t ix = static_cast<size_t>(qrow + tok) * p.hq + kg.g * p.G + (r % p.G);
+                            const float l = __ldg(p.lse + ix);
+                            l2[j] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
+                            nd[j] = -__ldg(p.Dvec + ix);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        sLse[b * 128 + lane + 32 * j] = l2[j];
+                        sD[b * 128 + lane + 32 * j] = nd[j];
+                    }
+                    mbar_arrive(&bars.row_full[b]);
+                }
+            }
+        }
     } else if (warp == 10) {
         // ------------------------------------------------------------ dQ flush
         // Lane 0: once both gradient warpgroups have staged dQ of a query tile
@@ -511,9 +542,9 @@ __global__ void __launch_bounds__(352, 1)
                     const int32_t p_first = t.q_start + tok0;
                     const int32_t qrow0 = t.row0 + tok0;
                     const uint32_t st = qt % C::kQStages;
-                    const float *lse_b = sLse + st * 128;
-                    const float *nd_b = sD + st * 128;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_full[st], (qt / C::kQStages) & 1, wd));
+                    const float *lse_b = sLse + (qt & 1) * 128;
+                    const float *nd_b = sD + (qt & 1) * 128;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_full[qt & 1], (qt >> 1) & 1, wd));
                     if (!ok) break;
                     // visible rows for this key: tile rows r (token r / G) with
                     // r_lo <= r < r_hi, i.e. p >= key position and the token inside the task
@@ -605,6 +636,7 @@ __global__ void __launch_bounds__(352, 1)
                         tmem_st_wait();
                     }
                     if (!ok) break;
+                    mbar_arrive(&bars.row_empty[qt & 1]);  // row statistics of this tile no longer read
                     fence_view_async_shared();
                     tc_fence_before();
                     mbar_arrive(&bars.ds_full);
@@ -696,7 +728,7 @@ cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtens
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_bwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, 352, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
+    kern<<<grid, 384, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
     return cudaGetLastError();
 }
 
