@@ -270,6 +270,69 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def measure_split_kv(args, dev, stream, pk):
+    """Partial prefill with split KV: 4096 new tokens at positions
+    131072..135167, the 135168-key context cut into 8 contiguous blocks, one
+    CA-task per block (float32 partial O, LSE), then ca_merge.  Reports the
+    forward over the blocks (TFLOP/s, 4 d FLOPs per causal pair per query
+    head) and the merge against the measured HBM bandwidth (algorithmic bytes:
+    every partial O and LSE read once, O (bf16) and LSE written once)."""
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    wsplit = W.split_kv_prefill(seed=args.seed)
+    whole = W.split_kv_prefill(seed=args.seed, split=False)
+    nb = wsplit.n_tasks
+    q, k, v, _ = W.make_tensors(whole, device=dev, need_grad_inputs=False)
+    nq, hq, d = q.shape
+    q8 = q.repeat(nb, 1, 1)  # the blocks share the query rows; tasks are packed one after another
+    plan = ca.Plan.from_workload(wsplit, o_dtype=ca.CA_DTYPE_FP32, stream=stream)
+    info = plan.info()
+    ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    o_p, lse_p = ca.alloc_forward(plan, device=dev)
+    o = torch.empty((nq, hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((nq, hq), dtype=torch.float32, device=dev)
+    parts_o = [o_p[b * nq:(b + 1) * nq] for b in range(nb)]
+    parts_l = [lse_p[b * nq:(b + 1) * nq] for b in range(nb)]
+    sh = stream.cuda_stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step():
+        plan.forward(q8, k, v, o_p, lse_p, ws, stream=sh)
+        ev[1].record(stream)
+        ca.merge(parts_o, parts_l, nq, hq, d, o, lse, parts_dtype=ca.CA_DTYPE_FP32,
+                 out_dtype=ca.CA_DTYPE_BF16, stream=sh)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    fwd_ms, merge_ms = [], []
+    for _ in range(args.steps):
+        ev[0].record(stream)
+        step()
+        ev[2].record(stream)
+        stream.synchronize()
+        fwd_ms.append(ev[0].elapsed_time(ev[1]))
+        merge_ms.append(ev[1].elapsed_time(ev[2]))
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the split-KV measurement")
+    f_ms, m_ms = float(np.median(fwd_ms)), float(np.median(merge_ms))
+    merge_bytes = nb * nq * hq * (d * 4 + 4) + nq * hq * (d * 2 + 4)
+    hbm = float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    gbs = merge_bytes / (m_ms * 1e-3) / 1e9
+    out = {
+        "workload": wsplit.name, "blocks": nb, "forward_ms": f_ms, "merge_ms": m_ms,
+        "forward_tflops": info["flops_fwd"] / (f_ms * 1e-3) / 1e12,
+        "forward_plus_merge_tflops": info["flops_fwd"] / ((f_ms + m_ms) * 1e-3) / 1e12,
+        "merge_roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                           "traffic": None, "algorithmic_bytes": merge_bytes},
+    }
+    plan.close()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local):
@@ -343,6 +406,9 @@ def run_gpu(args, rank, world, local):
         e2e = measure_e2e(args, plan, stream, (q, k, v, do), (o, lse), (dq, dk, dv), ws, world, flops_step)
 
     pk, pk_kind = peaks()
+    split_kv = None
+    if not args.no_split_kv:
+        split_kv = measure_split_kv(args, dev, stream, pk)
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
     peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     main_tf = info["flops_bwd"] / (main_ms * 1e-3) / 1e12
@@ -386,6 +452,7 @@ def run_gpu(args, rank, world, local):
                          "peak_kind": f"bf16 burst, {pk_kind}",
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
             "e2e": e2e,
+            "split_kv_prefill": split_kv,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -397,7 +464,7 @@ def run_gpu(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
@@ -405,6 +472,7 @@ def main():
                     help="causal pairs per head of the oracle's sample (bounds its CPU time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-split-kv", action="store_true", help="skip the split-KV prefill + merge measurement")
     ap.add_argument("--tokens", type=int, default=65536,
                     help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()
