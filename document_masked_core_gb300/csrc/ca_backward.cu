@@ -37,7 +37,9 @@ using namespace dev;
 // ------------------------------------------------------------------ preprocess
 template <bool O_F32>
 __global__ void __launch_bounds__(256) ca_bwd_pre_kernel(const void *o, const __nv_bfloat16 *d_o, float *D,
-                                                          float *dq_acc, int64_t units, int32_t d) {
+                                                          float *dq_acc, int64_t units, int32_t d,
+                                                          int32_t *sched) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;  // work queue of the main kernel
     const int32_t tpu = d / 8;  // 8 or 16 threads per (row, head), a power of two dividing 32
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t unit = gtid / tpu;
@@ -102,6 +104,7 @@ struct BwdParams {
     float scale_log2;  // softmax scale * log2(e)
     const float *lse;  // [total_q, hq]
     const float *Dvec; // [total_q, hq]
+    int32_t *sched;    // work-queue counter (zeroed by the preprocess kernel)
     __nv_bfloat16 *dk, *dv;
     DevCtl ctl;
 };
@@ -120,7 +123,8 @@ struct BwdCfg {
     static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
     // No alignment slack: the dynamic shared window starts 1024-byte aligned
     // (checked at kernel entry).  At least 120 KB so one CTA runs per SM.
-    static constexpr int kSmemRaw = kOffBar + 256;
+    static constexpr int kBarBytes = 512;  // BwdBars (checked below)
+    static constexpr int kSmemRaw = kOffBar + kBarBytes;
     static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;
     static_assert(kSmemBytes <= 232448, "backward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
@@ -142,6 +146,9 @@ struct BwdCfg {
     }
 };
 
+// warps that read each ring entry: MMA, 8 gradient, flush, row statistics
+constexpr uint32_t kRingConsumers = 11;
+
 struct BwdBars {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2];    // Q tile (and its row statistics) of stage s
@@ -152,9 +159,15 @@ struct BwdBars {
     // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
     // written by warpgroup 1 land in columns warpgroup 0 reads
     uint64_t s_loaded, dp_loaded;
+    // work queue: the producer takes the next item from the global counter and
+    // publishes it to the other roles through a 4-entry ring
+    uint64_t ring_full[4], ring_empty[4];
+    int32_t ring[4];
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
+
+static_assert(sizeof(BwdBars) <= 512, "barrier block exceeds its shared-memory reservation");
 
 struct KvGeo {
     int32_t doc, g, jt, n_q, kv_off, doc_len, t_begin, t_end;
@@ -262,6 +275,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(&bars.s_loaded, 256);
         mbar_init(&bars.dp_loaded, 256);
+        for (int r = 0; r < 4; ++r) {
+            mbar_init(&bars.ring_full[r], 1);
+            mbar_init(&bars.ring_empty[r], kRingConsumers);
+        }
         bars.abort_flag = 0;
         fence_mbar_init();
     }
@@ -287,7 +304,19 @@ __global__ void __launch_bounds__(384, 1)
         {
             uint32_t act = 0, qt = 0;
             bool ok = true;
-            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            for (uint32_t r = 0; ok; ++r) {
+                // take the next item and publish it to the other roles
+                int32_t idx = -1;
+                if (lane == 0) {
+                    ok = mbar_wait(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1, wd);
+                    if (ok) idx = atomicAdd(p.sched, 1);
+                    if (idx >= p.n_items) idx = -1;
+                    bars.ring[r & 3] = idx;
+                    mbar_arrive(&bars.ring_full[r & 3]);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                idx = __shfl_sync(0xffffffffu, idx, 0);
+                if (!ok || idx < 0) break;
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 if (lane == 0) {
@@ -362,7 +391,11 @@ __global__ void __launch_bounds__(384, 1)
                 umma_commit(&bars.s_full);
                 return true;
             };
-            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            for (uint32_t r = 0; ok; ++r) {
+                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                mbar_arrive(&bars.ring_empty[r & 3]);
+                if (idx < 0) break;
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
@@ -426,7 +459,13 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t qt = 0;
         bool ok = true;
         const float log2_scale = lg2(p.scale);
-        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+        for (uint32_t r = 0; ok; ++r) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
+            if (!ok) break;
+            const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
+            if (idx < 0) break;
             const KvGeo kg = decode_kv(p, idx);
             if (kg.n_q == 0) continue;
             for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
@@ -472,7 +511,11 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             uint32_t qt = 0;
             bool ok = true;
-            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            for (uint32_t r = 0; ok; ++r) {
+                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                mbar_arrive(&bars.ring_empty[r & 3]);
+                if (idx < 0) break;
                 const KvGeo kg = decode_kv(p, idx);
                 if (kg.n_q == 0) continue;
                 for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
@@ -514,7 +557,13 @@ __global__ void __launch_bounds__(384, 1)
         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
         uint32_t qt = 0;
         bool ok = true;
-        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+        for (uint32_t r = 0; ok; ++r) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
+            if (!ok) break;
+            const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
+            if (idx < 0) break;
             const KvGeo kg = decode_kv(p, idx);
             const int32_t kpos = kg.jt * kTileKeys + static_cast<int32_t>(i);  // this thread's key
             const bool key_in_doc = kpos < kg.doc_len;
@@ -741,6 +790,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     float *dq_acc = static_cast<float *>(workspace);
     float *Dvec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                             (units * pl->d * 4 + 255) / 256 * 256);
+    int32_t *sched = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(Dvec) + (units * 4 + 255) / 256 * 256);
     // 1. D = rowsum(dO * O), dQ accumulator = 0
     {
         cudaError_t e0 = mark(pl, 2, stream);
@@ -749,10 +799,10 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
         if (pl->o_dtype == CA_DTYPE_FP32)
             ca_bwd_pre_kernel<true><<<blocks, 256, 0, stream>>>(o, static_cast<const __nv_bfloat16 *>(d_o), Dvec,
-                                                                dq_acc, units, pl->d);
+                                                                dq_acc, units, pl->d, sched);
         else
             ca_bwd_pre_kernel<false><<<blocks, 256, 0, stream>>>(o, static_cast<const __nv_bfloat16 *>(d_o), Dvec,
-                                                                 dq_acc, units, pl->d);
+                                                                 dq_acc, units, pl->d, sched);
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess) e = mark(pl, 3, stream);
         if (e != cudaSuccess) return e;
@@ -780,6 +830,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     prm.scale_log2 = pl->scale * 1.4426950408889634f;
     prm.lse = lse;
     prm.Dvec = Dvec;
+    prm.sched = sched;
     prm.dk = static_cast<__nv_bfloat16 *>(dk);
     prm.dv = static_cast<__nv_bfloat16 *>(dv);
     prm.ctl.err = pl->d_err;

@@ -58,7 +58,8 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    static constexpr int kSmemRaw = kOffBar + 512;
+    static constexpr int kBarBytes = 512;  // FwdBars (checked below)
+    static constexpr int kSmemRaw = kOffBar + kBarBytes;
     static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;  // one CTA per SM
     static_assert(kSmemBytes <= 232448, "forward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
@@ -80,6 +81,8 @@ struct FwdBars {
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
+
+static_assert(sizeof(FwdBars) <= 512, "barrier block exceeds its shared-memory reservation");
 
 struct TileGeo {
     int32_t row0, p_first, ntok, n_kv;  // n_kv = 0: tile absent or sees nothing

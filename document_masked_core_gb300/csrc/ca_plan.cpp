@@ -310,11 +310,12 @@ ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64
     }
     p->n_bwd = static_cast<int64_t>(bwd.size());
 
-    // workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned
+    // workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned, then 256
+    // bytes of work-queue counters
     const int64_t rows_heads = p->total_q * p->hq;
     const int64_t dq_bytes = (rows_heads * p->d * 4 + 255) / 256 * 256;
     const int64_t d_bytes = (rows_heads * 4 + 255) / 256 * 256;
-    p->workspace_bytes = dq_bytes + d_bytes;
+    p->workspace_bytes = dq_bytes + d_bytes + 256;
     return CA_OK;
 }
 
