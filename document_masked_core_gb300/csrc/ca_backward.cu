@@ -790,7 +790,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     float *dq_acc = static_cast<float *>(workspace);
     float *Dvec = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                             (units * pl->d * 4 + 255) / 256 * 256);
-    int32_t *sched = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(Dvec) + (units * 4 + 255) / 256 * 256);
+    int32_t *sched = work_counters(pl, workspace);
     // 1. D = rowsum(dO * O), dQ accumulator = 0
     {
         cudaError_t e0 = mark(pl, 2, stream);

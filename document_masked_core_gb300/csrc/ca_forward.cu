@@ -1,6 +1,7 @@
 // Forward core attention over a rebatched pool of CA-tasks (sm_103a).
 //
-// One persistent CTA per SM walks the plan's forward items (longest first).
+// One persistent CTA per SM takes the plan's forward items (longest first)
+// from a global work queue.
 // An item is two consecutive 128-row query tiles A and B of one task and one
 // kv head g; a tile row is one (token, head) pair, 128 / G tokens x G heads,
 // so one 128-key K/V tile of head g serves both tiles (GQA sharing by packing
@@ -46,6 +47,7 @@ struct FwdParams {
     float scale_log2;  // softmax_scale * log2(e)
     void *o;
     float *lse;
+    int32_t *sched;  // work-queue counter (zeroed before the launch)
     DevCtl ctl;
 };
 
@@ -72,7 +74,12 @@ struct FwdCfg {
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 
+// warps that read each work-queue ring entry: MMA and the 8 softmax warps
+constexpr uint32_t kRingConsumers = 9;
+
 struct FwdBars {
+    uint64_t ring_full[4], ring_empty[4];
+    int32_t ring[4];
     uint64_t q_full[2], q_empty[2];
     uint64_t k_full[2], v_full[2], kv_empty[2];
     uint64_t s_full[2], p_full[2];
@@ -184,6 +191,10 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&bars.kv_empty[s], 1);
         }
         mbar_init(&bars.mma_done, 1);
+        for (int r = 0; r < 4; ++r) {
+            mbar_init(&bars.ring_full[r], 1);
+            mbar_init(&bars.ring_empty[r], kRingConsumers);
+        }
         bars.abort_flag = 0;
         fence_mbar_init();
     }
@@ -207,7 +218,14 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, q_it[2] = {0, 0};
             bool ok = true;
-            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            for (uint32_t r = 0; ok; ++r) {
+                // take the next item and publish it to the other roles
+                if (!(ok = mbar_wait(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1, wd))) break;
+                int32_t idx = atomicAdd(p.sched, 1);
+                if (idx >= p.n_items) idx = -1;
+                bars.ring[r & 3] = idx;
+                mbar_arrive(&bars.ring_full[r & 3]);
+                if (idx < 0) break;
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
 #pragma unroll
@@ -262,7 +280,11 @@ __global__ void __launch_bounds__(320, 1)
                 umma_commit(&bars.s_full[x]);
                 return true;
             };
-            for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+            for (uint32_t r = 0; ok; ++r) {
+                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                mbar_arrive(&bars.ring_empty[r & 3]);
+                if (idx < 0) break;
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
                 const int32_t nk[2] = {gi.t[0].n_kv, gi.t[1].n_kv};
@@ -321,7 +343,13 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t o_addr = tmem + lane_addr + C::kColO + x * D;
         uint32_t s_it = 0, o_it = 0;
         bool ok = true;
-        for (int32_t it = 0, idx = snake_item(0); idx < p.n_items && ok; idx = snake_item(++it)) {
+        for (uint32_t r = 0; ok; ++r) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
+            if (!ok) break;
+            const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
+            if (idx < 0) break;
             const ItemGeo gi = decode_item(p, idx);
             const TileGeo tg = gi.t[x];
             const int32_t tok = row / p.G;
@@ -480,8 +508,11 @@ cudaError_t launch_fwd_t(const ca_plan *pl, const CUtensorMap &tq, const CUtenso
 }  // namespace
 
 cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, const void *v, void *o, float *lse,
-                           cudaStream_t stream) {
+                           void *workspace, cudaStream_t stream) {
     if (pl->n_fwd == 0) return cudaSuccess;
+    int32_t *sched = work_counters(pl, workspace) + 1;
+    cudaError_t e0 = cudaMemsetAsync(sched, 0, sizeof(int32_t), stream);
+    if (e0 != cudaSuccess) return e0;
     CUtensorMap tq, tk, tv;
     if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
         make_tmap_3d(&tk, k, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK ||
@@ -497,6 +528,7 @@ cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, cons
     prm.scale_log2 = pl->scale * 1.4426950408889634f;
     prm.o = o;
     prm.lse = lse;
+    prm.sched = sched;
     prm.ctl.err = pl->d_err;
     prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
     const bool f32 = pl->o_dtype == CA_DTYPE_FP32;

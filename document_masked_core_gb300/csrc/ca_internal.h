@@ -96,8 +96,16 @@ inline cudaError_t mark(const ca_plan *p, int slot, cudaStream_t stream) {
     return cudaEventRecord(static_cast<cudaEvent_t>(p->timing_events[slot]), stream);
 }
 
+// Work-queue counters at the end of the workspace (256 bytes after the fp32
+// dQ accumulator and the D vector): [0] backward main kernel, [1] forward.
+inline int32_t *work_counters(const ca_plan *p, void *workspace) {
+    const int64_t units = p->total_q * p->hq;
+    const int64_t off = (units * p->d * 4 + 255) / 256 * 256 + (units * 4 + 255) / 256 * 256;
+    return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + off);
+}
+
 cudaError_t launch_forward(const ca_plan *p, const void *q, const void *k, const void *v, void *o,
-                           float *lse, cudaStream_t stream);
+                           float *lse, void *workspace, cudaStream_t stream);
 cudaError_t launch_backward(const ca_plan *p, const void *q, const void *k, const void *v, const void *o,
                             const float *lse, const void *d_o, void *dq, void *dk, void *dv,
                             void *workspace, cudaStream_t stream);

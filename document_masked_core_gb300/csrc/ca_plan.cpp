@@ -426,14 +426,13 @@ ca_status_t ca_plan_set_timing_events(ca_plan_t *p, void *const *events, int32_t
 
 ca_status_t ca_forward(const ca_plan_t *p, const void *q, const void *k, const void *v, void *o, float *lse,
                        void *workspace, void *stream) {
-    (void)workspace;
     if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
-    if (!q || !k || !v || !o || !lse) return fail(CA_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return fail(CA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (!q || !k || !v || !o || !lse || !workspace) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+        return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (o == q || o == k || o == v || static_cast<void *>(lse) == o)
         return fail(CA_ERR_INVALID_ARG, "outputs alias inputs");
-    cudaError_t e = launch_forward(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_forward(p, q, k, v, o, lse, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return CA_OK;
 }

@@ -26,14 +26,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 
-// k-th work item of this CTA in "snake" order over a longest-first list:
-// round r hands items r*grid .. r*grid+grid-1 to the CTAs, reversing the
-// direction every other round so that each CTA's share evens out.
-__device__ __forceinline__ int32_t snake_item(int32_t k) {
-    const int32_t g = static_cast<int32_t>(gridDim.x), b = static_cast<int32_t>(blockIdx.x);
-    return k * g + ((k & 1) ? (g - 1 - b) : b);
-}
-
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

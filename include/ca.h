@@ -135,10 +135,10 @@ void ca_plan_destroy(ca_plan_t *plan);
  *   LSE_p = ln sum_{j visible} exp(scale q_p . k_j)  (natural log of the
  *   scaled scores, as in the merge appendix of the million-token paper);
  *   O_p = sum_j exp(scale q_p . k_j - LSE_p) v_j.
- * workspace: ca_plan_info().workspace_bytes bytes of device memory (may be
- * NULL when that is 0).  Asynchronous on stream; launch failures return
- * CA_ERR_CUDA.  Device-side watchdog/bounds failures are reported by
- * ca_device_status.
+ * workspace: ca_plan_info().workspace_bytes bytes of device memory (the
+ * forward uses a work-queue counter in it).  Asynchronous on stream; launch
+ * failures return CA_ERR_CUDA.  Device-side watchdog/bounds failures are
+ * reported by ca_device_status.
  */
 ca_status_t ca_forward(const ca_plan_t *plan, const void *q, const void *k, const void *v,
                        void *o, float *lse, void *workspace, void *stream);
