@@ -114,12 +114,17 @@ struct BwdCfg {
     static constexpr int kHalfBytes = 128 * 128;
     static constexpr int kTileBytes = (D / 64) * kHalfBytes;
     static constexpr int kQStages = 2;
+    // dS (128 keys x 128 q rows bf16, 32 KB) lives in the dO tile of its query
+    // tile once dV has read that tile, when the tile is large enough (D = 128);
+    // otherwise in a buffer of its own.
+    static constexpr bool kDsInDo = kTileBytes >= 2 * kHalfBytes;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffQ = kOffV + kTileBytes;
     static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
-    static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;  // dS, 128 keys x 128 q rows bf16
-    static constexpr int kOffRow = kOffDS + 2 * kHalfBytes;          // LSE2[2][128], D[2][128]
+    static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;    // own dS buffer (D = 64 only)
+    static constexpr int kOffStg = kOffDS + (kDsInDo ? 0 : 2 * kHalfBytes);  // dQ staging, 2 boxes
+    static constexpr int kOffRow = kOffStg + 2 * kHalfBytes;         // LSE2[2][128], D[2][128]
     static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
     // No alignment slack: the dynamic shared window starts 1024-byte aligned
     // (checked at kernel entry).  At least 120 KB so one CTA runs per SM.
@@ -136,26 +141,36 @@ struct BwdCfg {
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);    // TMEM A x MN-major B
     static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
     // dQ staging for the TMA reduction: D/32 boxes of 32 fp32 columns x 128
-    // rows (16 KB each, 128-byte swizzle).  Columns 0 .. D/2-1 (warpgroup 0)
-    // go to the Q tile, columns D/2 .. D-1 (warpgroup 1) to the dO tile of
-    // the query tile just finished (the MMAs no longer read either); the two
-    // regions are released to the producer separately.
+    // rows (16 KB each, 128-byte swizzle).  With dS in the dO tile, boxes 0
+    // and 1 go there too (dQ, the last reader of dS, has completed); the
+    // others go to the staging buffer.  The Q tile is not used, so it returns
+    // to the producer as soon as dK has read it.
+    static constexpr int kDoBoxes = kDsInDo ? 2 : 0;
+    static_assert(D / 32 - kDoBoxes == 2, "staging buffer holds two boxes");
     __device__ static uint32_t stage_box_off(int b, uint32_t st) {
-        return b < D / 64 ? kOffQ + st * kTileBytes + b * kHalfBytes
-                          : kOffDO + st * kTileBytes + (b - D / 64) * kHalfBytes;
+        return b < kDoBoxes ? kOffDO + st * kTileBytes + b * kHalfBytes : kOffStg + (b - kDoBoxes) * kHalfBytes;
     }
+    __device__ static uint32_t ds_off(uint32_t st) { return kDsInDo ? kOffDO + st * kTileBytes : kOffDS; }
+    // Register split of the 512 threads (launch allocation 128 each):
+    // gradient warpgroups, the warpgroup of single-warp roles, dQ warpgroup.
+    static constexpr uint32_t kRegsGrad = 160, kRegsMisc = 88, kRegsDq = 104;
+    static_assert(2 * kRegsGrad + kRegsMisc + kRegsDq <= 4 * 128, "register split exceeds the launch allocation");
 };
 
-// warps that read each ring entry: MMA, 8 gradient, flush, row statistics
-constexpr uint32_t kRingConsumers = 11;
+// warps that read each ring entry: MMA, 8 gradient, flush, row statistics, 4 dQ
+constexpr uint32_t kRingConsumers = 15;
 
 struct BwdBars {
     uint64_t kv_full, kv_empty;
-    uint64_t q_full[2], q_empty[2];    // Q tile (and its row statistics) of stage s
-    uint64_t do_full[2], do_empty[2];  // dO tile of stage s
-    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, acc_empty, stg_full, mma_done;
-    uint64_t row_full[2];      // row statistics of query tile t (buffer t % 2) are in shared memory
-    uint64_t row_empty[2];     // the gradient warpgroups are done with buffer t % 2
+    uint64_t q_full[2], q_empty[2];    // Q tile of stage s (q_empty: committed after dK)
+    uint64_t do_full[2], do_empty[2];  // dO tile of stage s (do_empty: its dQ staging was read)
+    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, stg_full, mma_done;
+    uint64_t acc_full;      // dK, dV of the item are complete (committed after its last dK)
+    uint64_t acc_empty;     // the gradient warpgroups have read dK, dV out of TMEM
+    uint64_t dv_done;       // dV of the current tile has read the dO tile (dS may overwrite it)
+    uint64_t stg_empty;     // the staging buffer's boxes have been read by the reduction
+    uint64_t row_full[2];   // row statistics of query tile t (buffer t % 2) are in shared memory
+    uint64_t row_empty[2];  // the gradient warpgroups are done with buffer t % 2
     // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
     // written by warpgroup 1 land in columns warpgroup 0 reads
     uint64_t s_loaded, dp_loaded;
@@ -211,21 +226,25 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// Warp roles (384 threads): warps 0-7 gradient warpgroups, warp 8 TMA
-// producer, warp 9 TMEM owner + MMA issuer, warp 10 dQ flush, warp 11 row
-// statistics (LSE, D) of each query tile.
+// Warp roles (512 threads, four warpgroups):
+//   warps 0-7   gradient warpgroups (P^T, dS^T; dK/dV epilogue)
+//   warp 8      TMA producer          warp 9   TMEM owner + MMA issuer
+//   warp 10     dQ flush (TMA reduce) warp 11  row statistics (LSE, D)
+//   warps 12-15 dQ readout: TMEM -> shared staging
 // Per query tile t (in the order every role enumerates them):
-//   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO |
-//             [ds_full(t)] dK += dS^T Q, dQ = dS K (into the dP^T columns) |
-//             S^T(t+1) when the item has a next tile (S^T(first) at item start)
-//   gradient: P^T(t) -> p_full | dS^T(t) -> ds_full | dQ(t) -> registers ->
-//             dq_empty -> shared staging (the Q and dO tiles of tile t) ->
-//             stg_full
+//   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO -> dv_done |
+//             S^T(t+1) when the item has a next tile (S^T(first) at item start) |
+//             [ds_full(t)] dK += dS^T Q -> q_empty, dQ = dS K (into the dP^T columns)
+//   gradient: P^T(t) -> p_full | dS^T(t) (into the dO tile of t once dV has
+//             read it) -> ds_full, then straight on to P^T(t+1) (S^T(t+1) was
+//             issued while they computed dS^T(t))
+//   dQ warps: dQ(t) -> registers -> dq_empty -> staging in the dO tile of t
+//             and the staging buffer -> stg_full
 //   flush:    TMA reduce-adds of the staging into the fp32 accumulator; the
-//             Q tile is released (q_empty) once its half has been read, the
-//             dO tile (do_empty) once the other half has.
+//             dO tile is released (do_empty) once its boxes have been read,
+//             the staging buffer (stg_empty) once the others have.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     ca_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -240,10 +259,9 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t *sV = smem + C::kOffV;
     uint8_t *sQ = smem + C::kOffQ;
     uint8_t *sDO = smem + C::kOffDO;
-    uint8_t *sDS = smem + C::kOffDS;
     // row statistics of the query tile in each Q/dO stage, written by the
-    // producer warp: log2(e) LSE - log2(scale) (so exp2(scale log2(e) s - that)
-    // = scale P) and -D
+    // row-statistics warp: log2(e) LSE - log2(scale) (so exp2(scale log2(e) s
+    // - that) = scale P) and -D
     float *sLse = reinterpret_cast<float *>(smem + C::kOffRow);  // [2][128]
     float *sD = sLse + 256;                                        // [2][128]
     BwdBars &bars = *reinterpret_cast<BwdBars *>(smem + C::kOffBar);
@@ -265,10 +283,13 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bars.p_full, 256);
         mbar_init(&bars.ds_full, 256);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_empty, 256);
-        mbar_init(&bars.acc_empty, 256);
-        mbar_init(&bars.stg_full, 256);
+        mbar_init(&bars.dq_empty, 128);
+        mbar_init(&bars.stg_full, 128);
         mbar_init(&bars.mma_done, 1);
+        mbar_init(&bars.acc_full, 1);
+        mbar_init(&bars.acc_empty, 256);
+        mbar_init(&bars.dv_done, 1);
+        mbar_init(&bars.stg_empty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars.row_full[b], 32);
             mbar_init(&bars.row_empty[b], 256);
@@ -299,9 +320,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tmem = bars.tmem_base;
     const Watchdog wd{&p.ctl, &bars.abort_flag};
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ producer (lane 0 issues)
-        {
+    if (warp >= 8 && warp < 12) {
+        regs_decrease<C::kRegsMisc>();
+        if (warp == 8) {
+            // ------------------------------------------------------------ producer (lane 0 issues)
             uint32_t act = 0, qt = 0;
             bool ok = true;
             for (uint32_t r = 0; ok; ++r) {
@@ -338,21 +360,17 @@ __global__ void __launch_bounds__(384, 1)
                     task_tiles(t, kg.jt, p.tpt, first, count);
                     for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
                         const uint32_t st = qt % C::kQStages;
-                        if (lane == 0) ok = mbar_wait(&bars.q_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
-                        const int32_t tok0 = tile * p.tpt;
-                        const int32_t qrow = t.row0 + tok0;
-                        const int32_t ntok = min(p.tpt, t.q_len - tok0);
+                        const int32_t qrow = t.row0 + tile * p.tpt;
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(&bars.q_full[st], C::kTileBytes);
+                            ok = mbar_wait(&bars.q_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
+                            if (ok) {
+                                mbar_arrive_expect_tx(&bars.q_full[st], C::kTileBytes);
 #pragma unroll
-                            for (int h = 0; h < D / 64; ++h)
-                                tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[st],
-                                            h * 64, kg.g * p.G, qrow);
-                        }
-                        if (lane == 0) {
-                            ok = mbar_wait(&bars.do_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
+                                for (int h = 0; h < D / 64; ++h)
+                                    tma_load_3d(sQ + st * C::kTileBytes + h * C::kHalfBytes, &tm_q,
+                                                &bars.q_full[st], h * 64, kg.g * p.G, qrow);
+                            }
+                            if (ok) ok = mbar_wait(&bars.do_empty[st], ((qt / C::kQStages) & 1) ^ 1, wd);
                             if (ok) {
                                 mbar_arrive_expect_tx(&bars.do_full[st], C::kTileBytes);
 #pragma unroll
@@ -368,97 +386,198 @@ __global__ void __launch_bounds__(384, 1)
                 ++act;
             }
             if (!ok && lane == 0) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
-        }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t act = 0, qt = 0;
-            bool ok = true;
-            const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
-                           do_base = smem_u32(sDO), ds_base = smem_u32(sDS);
-            // S^T = K Q^T of the query tile in ring slot qi
-            auto issue_st = [&](uint32_t qi) -> bool {
-                const uint32_t st = qi % C::kQStages;
-                if (!mbar_wait(&bars.q_full[st], (qi / C::kQStages) & 1, wd)) return false;
-                tc_fence_after();
-                const uint32_t qb = q_base + st * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                    umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                            C::kIdescST, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&bars.s_full);
-                return true;
-            };
-            for (uint32_t r = 0; ok; ++r) {
-                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
-                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
-                mbar_arrive(&bars.ring_empty[r & 3]);
-                if (idx < 0) break;
-                const KvGeo kg = decode_kv(p, idx);
-                if (kg.n_q == 0) continue;
-                if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
-                tc_fence_after();
-                if (!(ok = issue_st(qt))) break;
-                for (int32_t j = 0; j < kg.n_q && ok; ++j, ++qt) {
-                    const uint32_t st = qt % C::kQStages;
-                    const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
-                    // dP^T = V dO^T, once dQ of the previous tile has left the dP^T columns
-                    if (!(ok = mbar_wait(&bars.do_full[st], (qt / C::kQStages) & 1, wd))) break;
-                    if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
+        } else if (warp == 9) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                uint32_t act = 0, qt = 0;
+                bool ok = true;
+                const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
+                               do_base = smem_u32(sDO), smem_base = smem_u32(smem);
+                // S^T = K Q^T of the query tile in ring slot qi
+                auto issue_st = [&](uint32_t qi) -> bool {
+                    const uint32_t st = qi % C::kQStages;
+                    if (!mbar_wait(&bars.q_full[st], (qi / C::kQStages) & 1, wd)) return false;
                     tc_fence_after();
+                    const uint32_t qb = q_base + st * C::kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                        umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                                sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                        umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024),
+                                sdesc_sw128(qb + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
                     }
-                    umma_commit(&bars.dp_full);
-                    // dV += P^T dO
-                    if (!(ok = mbar_wait(&bars.p_full, qt & 1, wd))) break;
-                    if (j == 0 && !(ok = mbar_wait(&bars.acc_empty, (act & 1) ^ 1, wd))) break;
+                    umma_commit(&bars.s_full);
+                    return true;
+                };
+                for (uint32_t r = 0; ok; ++r) {
+                    if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                    const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                    mbar_arrive(&bars.ring_empty[r & 3]);
+                    if (idx < 0) break;
+                    const KvGeo kg = decode_kv(p, idx);
+                    if (kg.n_q == 0) continue;
+                    if (!(ok = mbar_wait(&bars.kv_full, act & 1, wd))) break;
                     tc_fence_after();
+                    if (!(ok = issue_st(qt))) break;
+                    for (int32_t j = 0; j < kg.n_q && ok; ++j, ++qt) {
+                        const uint32_t st = qt % C::kQStages;
+                        const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
+                        // dP^T = V dO^T, once dQ of the previous tile has left the dP^T columns
+                        if (!(ok = mbar_wait(&bars.do_full[st], (qt / C::kQStages) & 1, wd))) break;
+                        if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                                sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                (j == 0 && kk == 0) ? 0u : 1u);
-                    // dK += dS^T Q ; dQ = dS K (into the dP^T columns)
-                    if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
-                    tc_fence_after();
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
+                            umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
+                                    sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&bars.dp_full);
+                        // dV += P^T dO
+                        if (!(ok = mbar_wait(&bars.p_full, qt & 1, wd))) break;
+                        if (j == 0 && !(ok = mbar_wait(&bars.acc_empty, (act & 1) ^ 1, wd))) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
-                                sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                (j == 0 && kk == 0) ? 0u : 1u);
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                                    sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                    (j == 0 && kk == 0) ? 0u : 1u);
+                        if (C::kDsInDo) umma_commit(&bars.dv_done);
+                        // S^T of the next query tile of this key tile: the P^T columns
+                        // are free once dV (issued above) has read them
+                        if (j + 1 < kg.n_q && !(ok = issue_st(qt + 1))) break;
+                        // dK += dS^T Q, then the Q tile goes back to the producer;
+                        // dQ = dS K (into the dP^T columns)
+                        if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_ss(tmem + C::kColDP, sdesc_sw128(ds_base + kk * 2048, C::kHalfBytes, 1024),
-                                sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
-                                kk > 0 ? 1u : 0u);
-                    umma_commit(&bars.dq_full);
-                    // S^T of the next query tile of this key tile
-                    if (j + 1 < kg.n_q && !(ok = issue_st(qt + 1))) break;
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                                    sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
+                                    (j == 0 && kk == 0) ? 0u : 1u);
+                        umma_commit(&bars.q_empty[st]);
+                        if (j + 1 == kg.n_q) umma_commit(&bars.acc_full);
+                        const uint32_t dsb = smem_base + C::ds_off(st);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ss(tmem + C::kColDP, sdesc_sw128(dsb + kk * 2048, C::kHalfBytes, 1024),
+                                    sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
+                                    kk > 0 ? 1u : 0u);
+                        umma_commit(&bars.dq_full);
+                    }
+                    if (!ok) break;
+                    umma_commit(&bars.kv_empty);
+                    ++act;
                 }
-                if (!ok) break;
-                umma_commit(&bars.kv_empty);
-                ++act;
+                umma_commit(&bars.mma_done);
+                const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
+                uint32_t zero = 0;
+                const Watchdog wd2{&drain, &zero};
+                mbar_wait(&bars.mma_done, 0, wd2);
             }
-            umma_commit(&bars.mma_done);
-            const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
-            uint32_t zero = 0;
-            const Watchdog wd2{&drain, &zero};
-            mbar_wait(&bars.mma_done, 0, wd2);
+            __syncwarp();
+        } else if (warp == 11) {
+            // ------------------------------------------------------------ row statistics
+            // All 32 lanes load LSE and D of each query tile's 128 rows from global
+            // memory into a 2-entry buffer ring, ahead of the gradient warpgroups.
+            uint32_t qt = 0;
+            bool ok = true;
+            const float log2_scale = lg2(p.scale);
+            for (uint32_t r = 0; ok; ++r) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
+                if (!ok) break;
+                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
+                if (idx < 0) break;
+                const KvGeo kg = decode_kv(p, idx);
+                if (kg.n_q == 0) continue;
+                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                    const DevTask t = p.tasks[p.doc_tasks[k]];
+                    int32_t first, count;
+                    task_tiles(t, kg.jt, p.tpt, first, count);
+                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                        const uint32_t b = qt & 1;
+                        ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_empty[b], ((qt >> 1) & 1) ^ 1, wd));
+                        if (!ok) break;
+                        const int32_t tok0 = tile * p.tpt;
+                        const int32_t qrow = t.row0 + tok0;
+                        const int32_t ntok = min(p.tpt, t.q_len - tok0);
+                        float l2[4], nd[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int32_t r = static_cast<int32_t>(lane) + 32 * j;
+                            const int32_t tok = r / p.G;
+                            l2[j] = INFINITY;
+                            nd[j] = 0.f;
+                            if (tok < ntok) {
+                                const size_t ix = static_cast<size_t>(qrow + tok) * p.hq + kg.g * p.G + (r % p.G);
+                                const float l = __ldg(p.lse + ix);
+                                l2[j] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
+                                nd[j] = -__ldg(p.Dvec + ix);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            sLse[b * 128 + lane + 32 * j] = l2[j];
+                            sD[b * 128 + lane + 32 * j] = nd[j];
+                        }
+                        mbar_arrive(&bars.row_full[b]);
+                    }
+                }
+            }
+        } else {
+            // ------------------------------------------------------------ dQ flush
+            // Lane 0: once the dQ warps have staged dQ of a query tile, add it
+            // into the fp32 accumulator with TMA reduce-adds; release the dO
+            // tile once its boxes have been read (the next dO load waits for
+            // it), then the staging buffer.
+            if (lane == 0) {
+                uint32_t qt = 0;
+                bool ok = true;
+                for (uint32_t r = 0; ok; ++r) {
+                    if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                    const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+                    mbar_arrive(&bars.ring_empty[r & 3]);
+                    if (idx < 0) break;
+                    const KvGeo kg = decode_kv(p, idx);
+                    if (kg.n_q == 0) continue;
+                    for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
+                        const DevTask t = p.tasks[p.doc_tasks[k]];
+                        int32_t first, count;
+                        task_tiles(t, kg.jt, p.tpt, first, count);
+                        for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
+                            const uint32_t st = qt % C::kQStages;
+                            if (!(ok = mbar_wait(&bars.stg_full, qt & 1, wd))) break;
+                            const int32_t qrow0 = t.row0 + tile * p.tpt;
+#pragma unroll
+                            for (int b = 0; b < C::kDoBoxes; ++b)
+                                tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
+                            bulk_commit_group();
+#pragma unroll
+                            for (int b = C::kDoBoxes; b < D / 32; ++b)
+                                tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
+                            bulk_commit_group();
+                            bulk_wait_group_read1();
+                            mbar_arrive(&bars.do_empty[st]);
+                            bulk_wait_group_read0();
+                            mbar_arrive(&bars.stg_empty);
+                        }
+                    }
+                }
+                bulk_wait_group0();  // every dQ reduction has completed before the CTA exits
+            }
         }
-        __syncwarp();
-    } else if (warp == 11) {
-        // ------------------------------------------------------------ row statistics
-        // All 32 lanes load LSE and D of each query tile's 128 rows from global
-        // memory into a 2-entry buffer ring, ahead of the gradient warpgroups.
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ dQ readout
+        // Lane i = q row i of the tile: dQ (fp32, D columns of the dP^T region)
+        // -> registers (64 columns at a time) -> the staging boxes; the TMEM
+        // columns are released as soon as the last columns are in registers,
+        // before waiting for the staging buffer.
+        regs_decrease<C::kRegsDq>();
+        const uint32_t i = threadIdx.x & 127u;
+        const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
         uint32_t qt = 0;
         bool ok = true;
-        const float log2_scale = lg2(p.scale);
         for (uint32_t r = 0; ok; ++r) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
             if (!ok) break;
@@ -473,89 +592,59 @@ __global__ void __launch_bounds__(384, 1)
                 int32_t first, count;
                 task_tiles(t, kg.jt, p.tpt, first, count);
                 for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
-                    const uint32_t b = qt & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_empty[b], ((qt >> 1) & 1) ^ 1, wd));
+                    const uint32_t st = qt % C::kQStages;
+                    const int32_t ntok = min(p.tpt, t.q_len - tile * p.tpt);
+                    const bool row_ok = static_cast<int32_t>(i / p.G) < ntok;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, qt & 1, wd));
                     if (!ok) break;
-                    const int32_t tok0 = tile * p.tpt;
-                    const int32_t qrow = t.row0 + tok0;
-                    const int32_t ntok = min(p.tpt, t.q_len - tok0);
-                    float l2[4], nd[4];
+                    tc_fence_after();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int32_t r = static_cast<int32_t>(lane) + 32 * j;
-                        const int32_t tok = r / p.G;
-                        l2[j] = INFINITY;
-                        nd[j] = 0.f;
-                        if (tok < ntok) {
-                            const size_t ix = static_cast<size_t>(qrow + tok) * p.hq + kg.g * p.G + (r % p.G);
-                            const float l = __ldg(p.lse + ix);
-                            l2[j] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f - log2_scale;
-                            nd[j] = -__ldg(p.Dvec + ix);
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t qr[2][32];
+                        const uint32_t q_addr = tmem + lane_addr + C::kColDP + 64 * h;
+                        tmem_ld32(q_addr, qr[0]);
+                        tmem_ld32(q_addr + 32, qr[1]);
+                        tmem_ld_wait();
+                        reg_fence(qr[0]);
+                        reg_fence(qr[1]);
+                        if (h == D / 64 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(&bars.dq_empty);
+                        }
+                        if (2 * h >= C::kDoBoxes) {  // boxes 2h, 2h+1 go to the staging buffer
+                            ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_empty, (qt & 1) ^ 1, wd));
+                            if (!ok) break;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint8_t *srow = smem + C::stage_box_off(2 * h + c, st) + i * 128;
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                const uint4 v = row_ok ? make_uint4(qr[c][4 * c8], qr[c][4 * c8 + 1],
+                                                                    qr[c][4 * c8 + 2], qr[c][4 * c8 + 3])
+                                                       : make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4 *>(srow + ((c8 ^ (i & 7)) * 16)) = v;
+                            }
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        sLse[b * 128 + lane + 32 * j] = l2[j];
-                        sD[b * 128 + lane + 32 * j] = nd[j];
-                    }
-                    mbar_arrive(&bars.row_full[b]);
+                    if (!ok) break;
+                    fence_view_async_shared();
+                    mbar_arrive(&bars.stg_full);
                 }
             }
-        }
-    } else if (warp == 10) {
-        // ------------------------------------------------------------ dQ flush
-        // Lane 0: once both gradient warpgroups have staged dQ of a query tile
-        // in its Q/dO stage, add it into the fp32 accumulator with TMA
-        // reduce-adds, wait until they have read the staging and release the
-        // stage to the producer.
-        if (lane == 0) {
-            uint32_t qt = 0;
-            bool ok = true;
-            for (uint32_t r = 0; ok; ++r) {
-                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
-                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
-                mbar_arrive(&bars.ring_empty[r & 3]);
-                if (idx < 0) break;
-                const KvGeo kg = decode_kv(p, idx);
-                if (kg.n_q == 0) continue;
-                for (int32_t k = kg.t_begin; k < kg.t_end && ok; ++k) {
-                    const DevTask t = p.tasks[p.doc_tasks[k]];
-                    int32_t first, count;
-                    task_tiles(t, kg.jt, p.tpt, first, count);
-                    for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
-                        const uint32_t st = qt % C::kQStages;
-                        if (!(ok = mbar_wait(&bars.stg_full, qt & 1, wd))) break;
-                        const int32_t qrow0 = t.row0 + tile * p.tpt;
-                        // the half staged in the Q tile first (the next Q load is needed
-                        // sooner, by S^T), then the half staged in the dO tile
-#pragma unroll
-                        for (int b = 0; b < D / 64; ++b)
-                            tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
-                        bulk_commit_group();
-#pragma unroll
-                        for (int b = D / 64; b < D / 32; ++b)
-                            tma_reduce_add_3d(&tm_dq, smem + C::stage_box_off(b, st), b * 32, kg.g * p.G, qrow0);
-                        bulk_commit_group();
-                        bulk_wait_group_read1();
-                        mbar_arrive(&bars.q_empty[st]);
-                        bulk_wait_group_read0();
-                        mbar_arrive(&bars.do_empty[st]);
-                    }
-                }
-            }
-            bulk_wait_group0();  // every dQ reduction has completed before the CTA exits
         }
     } else {
         // ------------------------------------------------------------ gradient warpgroups
         // Warpgroup w (warps 4w .. 4w+3) owns query rows / S^T columns
-        // 64w .. 64w+63 of every tile and head_dim columns D/2 w .. of dQ, dK, dV.
+        // 64w .. 64w+63 of every tile and head_dim columns D/2 w .. of dK, dV.
+        regs_increase<C::kRegsGrad>();
         const int wg = static_cast<int>(warp >> 2);
-        const uint32_t i = threadIdx.x & 127u;  // TMEM lane: key row of S^T, dP^T, dK, dV; q row of dQ
+        const uint32_t i = threadIdx.x & 127u;  // TMEM lane: key row of S^T, dP^T, dK, dV
         const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
         const int c0 = 64 * wg;
         const float inv_scale = 1.f / p.scale;
         const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-        uint32_t qt = 0;
+        uint32_t qt = 0, act = 0;
         bool ok = true;
         for (uint32_t r = 0; ok; ++r) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
@@ -589,8 +678,6 @@ __global__ void __launch_bounds__(384, 1)
                     const int32_t tok0 = tile * p.tpt;
                     const int32_t ntok = min(p.tpt, t.q_len - tok0);
                     const int32_t p_first = t.q_start + tok0;
-                    const int32_t qrow0 = t.row0 + tok0;
-                    const uint32_t st = qt % C::kQStages;
                     const float *lse_b = sLse + (qt & 1) * 128;
                     const float *nd_b = sD + (qt & 1) * 128;
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_full[qt & 1], (qt >> 1) & 1, wd));
@@ -658,7 +745,7 @@ __global__ void __launch_bounds__(384, 1)
                         reg_fence(dr[0]);
                         reg_fence(dr[1]);
                         mbar_arrive(&bars.dp_loaded);
-                        uint8_t *row = sDS + wg * C::kHalfBytes + i * 128;
+                        uint8_t *row = smem + C::ds_off(qt % C::kQStages) + wg * C::kHalfBytes + i * 128;
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {  // q rows 64w + 32c ..
                             if (c == 0) {
@@ -675,6 +762,14 @@ __global__ void __launch_bounds__(384, 1)
                                 pk[e / 2] = pack_bf16(x.x, x.y);
                             }
                             tmem_st16(dp_addr + 32 * wg + 16 * c, pk);
+                            if (c == 0) {
+                                // the dS buffer is free: dV has read the dO tile it
+                                // shares, or the previous dQ has read the own buffer
+                                ok = C::kDsInDo ? mbar_wait(&bars.dv_done, qt & 1, wd)
+                                                : mbar_wait(&bars.dq_full, (qt & 1) ^ 1, wd);
+                                ok = __all_sync(0xffffffffu, ok);
+                                if (!ok) break;
+                            }
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const int c8 = 4 * c + j;  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
@@ -689,42 +784,15 @@ __global__ void __launch_bounds__(384, 1)
                     fence_view_async_shared();
                     tc_fence_before();
                     mbar_arrive(&bars.ds_full);
-                    // ---- dQ (lane i = q row i, columns D/2 w ..): TMEM -> registers,
-                    // release the columns, stage in shared memory, one TMA reduce-add
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, qt & 1, wd));
-                    if (!ok) break;
-                    tc_fence_after();
-                    {
-                        const bool row_ok = static_cast<int32_t>(i / p.G) < ntok;
-                        uint32_t qr[D / 64][32];
-                        const uint32_t q_addr = tmem + lane_addr + C::kColDP + wg * (D / 2);
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c) tmem_ld32(q_addr + c * 32, qr[c]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c) reg_fence(qr[c]);
-                        tc_fence_before();
-                        mbar_arrive(&bars.dq_empty);
-#pragma unroll
-                        for (int c = 0; c < D / 64; ++c) {
-                            uint8_t *srow = smem + C::stage_box_off(wg * (D / 64) + c, st) + i * 128;
-#pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 v = row_ok ? make_uint4(qr[c][4 * c8], qr[c][4 * c8 + 1], qr[c][4 * c8 + 2],
-                                                                    qr[c][4 * c8 + 3])
-                                                       : make_uint4(0, 0, 0, 0);
-                                *reinterpret_cast<uint4 *>(srow + ((c8 ^ (i & 7)) * 16)) = v;
-                            }
-                        }
-                    }
-                    fence_view_async_shared();
-                    mbar_arrive(&bars.stg_full);
                 }
             }
             if (!ok) break;
-            // ---- epilogue: dK, dV of this key tile (lane i = key i, columns D/2 w ..);
-            // every MMA of the item completed before the last dq_full.  The dV
-            // accumulator holds scale dV (it summed P' = scale P).
+            // ---- epilogue: dK, dV of this key tile (lane i = key i, columns D/2 w ..)
+            // once the item's last dK has completed.  The dV accumulator holds
+            // scale dV (it summed P' = scale P).
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_full, act & 1, wd));
+            if (!ok) break;
+            tc_fence_after();
             {
                 const uint32_t dv_addr = tmem + lane_addr + C::kColDV + wg * (D / 2);
                 const uint32_t dk_addr = tmem + lane_addr + C::kColDK + wg * (D / 2);
@@ -756,6 +824,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars.acc_empty);
             }
+            ++act;
         }
     }
 
@@ -775,9 +844,20 @@ cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtens
     auto kern = ca_bwd_main_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register increases draw on the CTA's launch allocation
+    // (512 threads x registers per thread): refuse to launch a build whose
+    // allocation could not cover the split, where an increase would block.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * 4 < static_cast<int>(2 * C::kRegsGrad + C::kRegsMisc + C::kRegsDq)) {
+        set_error("backward main kernel was built with " + std::to_string(fa.numRegs) +
+                  " registers per thread, below its warpgroup register split");
+        return cudaErrorInvalidConfiguration;
+    }
     const int grid = static_cast<int>(std::min<int64_t>(pl->n_bwd, pl->num_sms));
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, 384, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
+    kern<<<grid, 512, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
     return cudaGetLastError();
 }
 
