@@ -137,6 +137,11 @@ struct BwdCfg {
     static constexpr uint32_t kColDP = 128;  // dP^T, then dS^T (bf16), then dQ (fp32, D columns)
     static constexpr uint32_t kColDV = 256;
     static constexpr uint32_t kColDK = 256 + D;
+    // Packed bf16 P^T / dS^T: warpgroup w writes its 64 q rows (two per
+    // column) to the first 32 of the 64 columns it read, so neither warpgroup
+    // overwrites columns the other has yet to load.  K step kk (q rows
+    // 16kk .. 16kk+15) of the dV / dK products starts at this column.
+    __host__ __device__ static constexpr uint32_t packed_col(int kk) { return 8 * kk + (kk >= 4 ? 32 : 0); }
     static constexpr uint32_t kIdescST = idesc_bf16(128, 128, false, false);  // K-major x K-major
     static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);    // TMEM A x MN-major B
     static constexpr uint32_t kIdescDQ = idesc_bf16(128, D, true, true);      // MN-major A x MN-major B
@@ -171,9 +176,6 @@ struct BwdBars {
     uint64_t stg_empty;     // the staging buffer's boxes have been read by the reduction
     uint64_t row_full[2];   // row statistics of query tile t (buffer t % 2) are in shared memory
     uint64_t row_empty[2];  // the gradient warpgroups are done with buffer t % 2
-    // both warpgroups have loaded S^T / dP^T: the packed bf16 P^T / dS^T
-    // written by warpgroup 1 land in columns warpgroup 0 reads
-    uint64_t s_loaded, dp_loaded;
     // work queue: the producer takes the next item from the global counter and
     // publishes it to the other roles through a 4-entry ring
     uint64_t ring_full[4], ring_empty[4];
@@ -294,8 +296,6 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&bars.row_full[b], 32);
             mbar_init(&bars.row_empty[b], 256);
         }
-        mbar_init(&bars.s_loaded, 256);
-        mbar_init(&bars.dp_loaded, 256);
         for (int r = 0; r < 4; ++r) {
             mbar_init(&bars.ring_full[r], 1);
             mbar_init(&bars.ring_empty[r], kRingConsumers);
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(512, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                            umma_ts(tmem + C::kColDV, tmem + C::kColS + C::packed_col(kk),
                                     sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
                                     (j == 0 && kk == 0) ? 0u : 1u);
                         if (C::kDsInDo) umma_commit(&bars.dv_done);
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(512, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8,
+                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + C::packed_col(kk),
                                     sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
                                     (j == 0 && kk == 0) ? 0u : 1u);
                         umma_commit(&bars.q_empty[st]);
@@ -700,7 +700,6 @@ __global__ void __launch_bounds__(512, 1)
                         tmem_ld_wait();
                         reg_fence(sr[0]);
                         reg_fence(sr[1]);
-                        mbar_arrive(&bars.s_loaded);
                         const float2 *l2p = reinterpret_cast<const float2 *>(lse_b + c0);
 #pragma unroll
                         for (int e = 0; e < 64; e += 2) {
@@ -721,11 +720,8 @@ __global__ void __launch_bounds__(512, 1)
                         uint32_t pk[32];
 #pragma unroll
                         for (int w = 0; w < 32; ++w) pk[w] = pack_bf16(pt[2 * w], pt[2 * w + 1]);
-                        if (!mbar_wait(&bars.s_loaded, qt & 1, wd)) ok = false;
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (ok) tmem_st32(s_addr + 32 * wg, pk);  // q rows 64w.. packed two per column
+                        tmem_st32(s_addr + c0, pk);  // q rows 64w.. packed two per column
                     }
-                    if (!ok) break;
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&bars.p_full);
@@ -744,15 +740,9 @@ __global__ void __launch_bounds__(512, 1)
                         tmem_ld_wait();
                         reg_fence(dr[0]);
                         reg_fence(dr[1]);
-                        mbar_arrive(&bars.dp_loaded);
                         uint8_t *row = smem + C::ds_off(qt % C::kQStages) + wg * C::kHalfBytes + i * 128;
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {  // q rows 64w + 32c ..
-                            if (c == 0) {
-                                if (!mbar_wait(&bars.dp_loaded, qt & 1, wd)) ok = false;
-                                ok = __all_sync(0xffffffffu, ok);
-                                if (!ok) break;
-                            }
                             uint32_t pk[16];
 #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
@@ -761,7 +751,7 @@ __global__ void __launch_bounds__(512, 1)
                                                             __fadd2_rn(d2, nd2[16 * c + e / 2]));
                                 pk[e / 2] = pack_bf16(x.x, x.y);
                             }
-                            tmem_st16(dp_addr + 32 * wg + 16 * c, pk);
+                            tmem_st16(dp_addr + c0 + 16 * c, pk);
                             if (c == 0) {
                                 // the dS buffer is free: dV has read the dO tile it
                                 // shares, or the previous dQ has read the own buffer
