@@ -19,7 +19,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libca.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ca_plan.cpp", "ca_forward.cu", "ca_backward.cu", "ca_merge.cu", "ca_noalloc.cu"]
+SOURCES = ["ca_plan.cpp", "ca_sched.cpp", "ca_forward.cu", "ca_backward.cu", "ca_merge.cu", "ca_noalloc.cu"]
 
 
 def nvcc() -> str:
@@ -33,6 +33,7 @@ def nvcc() -> str:
 def _deps_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(ROOT, "include", "ca.h"))
+    files.append(os.path.join(ROOT, "include", "ca_sched.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

@@ -26,11 +26,13 @@ CA_ERR_NO_DEVICE = 6
 CA_DTYPE_BF16 = 0
 CA_DTYPE_FP32 = 1
 
-# names declared in include/ca.h, in order
+# names declared in include/ca.h and include/ca_sched.h, in order
 EXPORTS = [
     "ca_plan_create", "ca_plan_dry_run", "ca_plan_info", "ca_plan_task_pairs", "ca_plan_destroy",
     "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
+    "ca_profile_create", "ca_profile_predict", "ca_profile_peak", "ca_profile_destroy", "ca_optimal_shard",
+    "ca_schedule",
 ]
 
 
@@ -57,6 +59,26 @@ class PlanInfo(ctypes.Structure):
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class SchedParams(ctypes.Structure):
+    _fields_ = [("n_servers", ctypes.c_int32), ("tolerance", ctypes.c_double), ("min_score", ctypes.c_double),
+                ("bytes_q", ctypes.c_double), ("bytes_kv", ctypes.c_double), ("min_shard_tokens", ctypes.c_int64)]
+
+
+class SchedTask(ctypes.Structure):
+    _fields_ = [("server", ctypes.c_int32), ("home", ctypes.c_int32), ("doc_id", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("q_start", ctypes.c_int64), ("q_len", ctypes.c_int64),
+                ("kv_len", ctypes.c_int64), ("pairs", ctypes.c_int64)]
+
+
+class SchedResult(ctypes.Structure):
+    _fields_ = [("target_pairs_x1000", ctypes.c_int64), ("max_load", ctypes.c_int64), ("min_load", ctypes.c_int64),
+                ("n_tasks", ctypes.c_int64), ("n_migrations", ctypes.c_int64), ("n_splits", ctypes.c_int64),
+                ("comm_bytes", ctypes.c_double)]
+
+    def as_dict(self):
+        return {n: (float(getattr(self, n)) if n == "comm_bytes" else int(getattr(self, n))) for n, _ in self._fields_}
 
 
 _lib = None
@@ -107,6 +129,21 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_last_error.argtypes = []
     L.ca_version.restype = i32
     L.ca_version.argtypes = []
+    dbl = ctypes.c_double
+    L.ca_profile_create.restype = st
+    L.ca_profile_create.argtypes = [vp, i32, vp, i32, vp, dbl, ctypes.POINTER(vp)]
+    L.ca_profile_predict.restype = st
+    L.ca_profile_predict.argtypes = [vp, i64, i64, ctypes.POINTER(dbl)]
+    L.ca_profile_peak.restype = st
+    L.ca_profile_peak.argtypes = [vp, ctypes.POINTER(dbl)]
+    L.ca_profile_destroy.restype = None
+    L.ca_profile_destroy.argtypes = [vp]
+    L.ca_optimal_shard.restype = st
+    L.ca_optimal_shard.argtypes = [i64, i64, dbl, i64, dbl, dbl, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                   ctypes.POINTER(dbl)]
+    L.ca_schedule.restype = st
+    L.ca_schedule.argtypes = [vp, i32, ctypes.POINTER(SchedParams), ctypes.POINTER(SchedTask), i64,
+                              ctypes.POINTER(SchedResult)]
     if path is None:
         _lib = L
     return L
@@ -273,3 +310,74 @@ def merge(o_parts: Sequence, lse_parts: Sequence, rows: int, heads: int, head_di
 
 def version() -> int:
     return int(load().ca_version())
+
+
+# ---------------------------------------------------------------- host planning (include/ca_sched.h)
+
+class Profile:
+    """Profiler cost model (ca_profile_*): measured fwd+bwd seconds on a grid
+    of (query length, context length) CA-task shapes."""
+
+    def __init__(self, nq_grid, nkv_grid, seconds, flops_per_pair: float):
+        L = load()
+        self.nq_grid = np.ascontiguousarray(nq_grid, dtype=np.int64)
+        self.nkv_grid = np.ascontiguousarray(nkv_grid, dtype=np.int64)
+        sec = np.ascontiguousarray(seconds, dtype=np.float64).reshape(len(self.nq_grid), len(self.nkv_grid))
+        h = ctypes.c_void_p()
+        _check(L.ca_profile_create(self.nq_grid.ctypes.data, len(self.nq_grid), self.nkv_grid.ctypes.data,
+                                   len(self.nkv_grid), sec.ctypes.data, float(flops_per_pair), ctypes.byref(h)))
+        self._h = h
+
+    def predict(self, n_q: int, n_kv: int) -> float:
+        out = ctypes.c_double()
+        _check(load().ca_profile_predict(self._h.value, int(n_q), int(n_kv), ctypes.byref(out)))
+        return float(out.value)
+
+    def peak(self) -> float:
+        out = ctypes.c_double()
+        _check(load().ca_profile_peak(self._h.value, ctypes.byref(out)))
+        return float(out.value)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().ca_profile_destroy(self._h.value)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def optimal_shard(L_q: int, L_kv: int, alpha: float, target_pairs: int, bytes_q: float, bytes_kv: float):
+    """ca_optimal_shard: (n_q, n_kv, continuous optimum) of a split."""
+    nq, nkv, real = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+    _check(load().ca_optimal_shard(int(L_q), int(L_kv), float(alpha), int(target_pairs), float(bytes_q),
+                                   float(bytes_kv), ctypes.byref(nq), ctypes.byref(nkv), ctypes.byref(real)))
+    return int(nq.value), int(nkv.value), float(real.value)
+
+
+def schedule(doc_len, n_servers: int, bytes_q: float, bytes_kv: float, tolerance: float = 0.0,
+             min_score: float = 0.0, min_shard_tokens: int = 0):
+    """ca_schedule: returns (tasks as a structured numpy array, result dict)."""
+    L = load()
+    dl = np.ascontiguousarray(doc_len, dtype=np.int64)
+    prm = SchedParams(int(n_servers), float(tolerance), float(min_score), float(bytes_q), float(bytes_kv),
+                      int(min_shard_tokens))
+    res = SchedResult()
+    cap = max(16, 4 * len(dl) + 4 * n_servers)
+    while True:
+        buf = (SchedTask * cap)()
+        st = L.ca_schedule(dl.ctypes.data, len(dl), ctypes.byref(prm), buf, cap, ctypes.byref(res))
+        if st == CA_OK:
+            break
+        if st == CA_ERR_INVALID_ARG and res.n_tasks > cap:
+            cap = int(res.n_tasks)
+            continue
+        _check(st)
+    n = int(res.n_tasks)
+    dt = np.dtype([("server", np.int32), ("home", np.int32), ("doc_id", np.int32), ("reserved", np.int32),
+                   ("q_start", np.int64), ("q_len", np.int64), ("kv_len", np.int64), ("pairs", np.int64)])
+    tasks = np.frombuffer(bytes(buf)[: n * ctypes.sizeof(SchedTask)], dtype=dt).copy()
+    return tasks, res.as_dict()

@@ -1,4 +1,4 @@
-"""Host-side checks of libca.so that need no GPU: every symbol include/ca.h
+"""Host-side checks of libca.so that need no GPU: every symbol include/*.h
 declares is exported, the integer accounting of the plan equals the oracle's
 enumeration bit-exactly, and invalid descriptors are rejected."""
 import ctypes
@@ -22,9 +22,13 @@ def built():
 
 
 def declared_symbols():
-    text = open(os.path.join(ROOT, "include", "ca.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ca_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ca_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_symbol():

@@ -1,0 +1,301 @@
+"""Host planning (include/ca_sched.h) on the CPU: the oracle in
+oracle/sched.py pinned by brute force, closed forms and a schedule worked by
+hand; the library's C++ matched to it exactly; the multi-server path run as
+two gloo ranks that agree on one schedule and split it between them."""
+import math
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+from document_masked_core_gb300 import build, capi
+from oracle import sched as O
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+
+
+def doc_sets():
+    rng = np.random.default_rng(7)
+    sets = {
+        "llama8b_64k": [int(x) for x in W.llama8b_chunk(seed=0).doc_len],
+        "llama8b_64k_s3": [int(x) for x in W.llama8b_chunk(seed=3).doc_len],
+        "uniform_16": [int(x) for x in rng.integers(8192, 131072, 16, endpoint=True)],
+        "long_512k": [int(x) for x in W.long_context_chunk().doc_len],
+        "tiny": [1024, 512, 256, 256],
+        "one_doc": [65536],
+    }
+    return sets
+
+
+def as_tuples(tasks):
+    return [(int(t["server"]), int(t["home"]), int(t["doc_id"]), int(t["q_start"]), int(t["q_len"]),
+             int(t["kv_len"]), int(t["pairs"])) for t in tasks]
+
+
+# ---------------------------------------------------------------- pins of the oracle
+
+def test_shard_pairs_closed_form_equals_enumeration():
+    for n_kv in range(1, 60):
+        for n_q in range(1, n_kv + 1):
+            brute = sum(p + 1 for p in range(n_kv - n_q, n_kv))
+            assert O.shard_pairs(n_q, n_kv) == brute
+            assert n_q * n_kv - n_q * (n_q - 1) // 2 == brute
+
+
+def test_split_optimum_is_the_brute_force_minimum():
+    """Appendix B: minimise n_q*bq + n_kv*bkv subject to the work fraction
+    constraint; the closed form projected onto the feasible interval equals a
+    dense search over n_q."""
+    rng = np.random.default_rng(1)
+    for _ in range(300):
+        L_kv = int(rng.integers(2, 200000))
+        L_q = int(rng.integers(1, L_kv + 1))
+        alpha = float(rng.uniform(0.001, 1.0))
+        bq, bkv = float(rng.uniform(0.5, 4.0)), float(rng.uniform(0.1, 4.0))
+        n_real, lo, hi = O.optimal_shard_real(L_q, L_kv, alpha, bq, bkv)
+        A = alpha * L_q * (2 * L_kv - L_q)
+        grid = np.linspace(max(lo, 1e-9), max(hi, lo), 20001)
+        n_kv = (A / grid + grid) / 2
+        ok = (n_kv <= L_kv * (1 + 1e-12)) & (n_kv - grid >= (L_kv - L_q) * (1 - 1e-12) - 1e-9) & (grid <= L_q + 1e-9)
+        comm = np.where(ok, grid * bq + n_kv * bkv, np.inf)
+        best = grid[int(np.argmin(comm))]
+        step = (max(hi, lo) - max(lo, 1e-9)) / 20000 + 1e-9
+        assert abs(best - n_real) <= 2 * step + 1e-9 * max(1.0, n_real), (L_q, L_kv, alpha, best, n_real)
+        # the constraint holds at the optimum
+        nk = (A / n_real + n_real) / 2
+        assert nk <= L_kv * (1 + 1e-9) and nk - n_real >= (L_kv - L_q) - 1e-6 * L_kv
+
+
+def test_unconstrained_optimum_when_interior():
+    """Interior case: the stationary point of n_q*bq + bkv*(A/n_q + n_q)/2."""
+    L_q, L_kv, alpha, bq, bkv = 4096, 65536, 0.3, 1.0, 0.5
+    n_real, lo, hi = O.optimal_shard_real(L_q, L_kv, alpha, bq, bkv)
+    A = alpha * L_q * (2 * L_kv - L_q)
+    f = lambda n: n * bq + bkv * (A / n + n) / 2  # noqa: E731
+    h = 1e-3
+    if lo < n_real < hi:
+        assert abs((f(n_real + h) - f(n_real - h)) / (2 * h)) < 1e-6
+
+
+def bilinear_grid():
+    nq = [128, 512, 2048, 8192]
+    nkv = [128, 1024, 8192, 65536]
+    a, b, c, d = 1e-5, 3e-8, 2e-9, 4e-13
+    sec = [[a + b * x + c * y + d * x * y for y in nkv] for x in nq]
+    return nq, nkv, sec, (a, b, c, d)
+
+
+def test_profile_interpolation_reproduces_a_bilinear_function():
+    nq, nkv, sec, (a, b, c, d) = bilinear_grid()
+    rng = np.random.default_rng(2)
+    for _ in range(500):
+        y = int(rng.integers(128, 65537))
+        x = int(rng.integers(128, min(8192, y) + 1))
+        got = O.profile_predict(nq, nkv, sec, 1.0, x, y)
+        assert got == pytest.approx(a + b * x + c * y + d * x * y, rel=1e-12)
+    for i, x in enumerate(nq):
+        for j, y in enumerate(nkv):
+            if x <= y:
+                assert O.profile_predict(nq, nkv, sec, 1.0, x, y) == pytest.approx(sec[i][j], rel=1e-15)
+    # below the first grid point: clamped to it
+    assert O.profile_predict(nq, nkv, sec, 1.0, 1, 100) == pytest.approx(sec[0][0], rel=1e-15)
+
+
+def test_profile_saturation_uses_peak_measured_throughput():
+    nq, nkv, sec, _ = bilinear_grid()
+    fpp = 12 * 128 * 32
+    best = 0.0
+    for i, x in enumerate(nq):
+        for j, y in enumerate(nkv):
+            q = min(x, y)
+            best = max(best, sum(p + 1 for p in range(y - q, y)) * fpp / sec[i][j])
+    assert O.profile_peak(nq, nkv, sec, fpp) == pytest.approx(best, rel=1e-12)
+    for x, y in [(16384, 100000), (100, 131072), (9000, 9000)]:
+        pairs = sum(p + 1 for p in range(y - x, y))
+        assert O.profile_predict(nq, nkv, sec, fpp, x, y) == pytest.approx(pairs * fpp / best, rel=1e-12)
+
+
+def read_hand_example():
+    path = os.path.join(ROOT, "tests", "golden", "sched_hand_example.txt")
+    tasks, stats, inp = [], {}, None
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = line.split()
+        if f[0] == "input":
+            inp = ([int(x) for x in f[1].split(",")], int(f[2]), float(f[3]), float(f[4]))
+        elif f[0] == "task":
+            tasks.append(tuple(int(x) for x in f[1:]))
+        elif f[0] == "stats":
+            stats = {kv.split("=")[0]: float(kv.split("=")[1]) for kv in f[1:]}
+    return inp, tasks, stats
+
+
+def test_oracle_schedule_matches_hand_worked_example():
+    (docs, k, bq, bkv), tasks, stats = read_hand_example()
+    got, st = O.schedule(docs, k, bq, bkv)
+    assert [tuple(t) for t in got] == tasks
+    for key, v in stats.items():
+        assert st[key] == v, key
+
+
+@pytest.mark.parametrize("name", list(doc_sets()))
+@pytest.mark.parametrize("k", [2, 3, 8])
+def test_oracle_schedule_invariants(name, k):
+    docs = doc_sets()[name]
+    eps = 0.01
+    tasks, st = O.schedule(docs, k, 8192.0, 4096.0, tolerance=eps)
+    # every query token of every document is covered exactly once, contexts are prefixes
+    per_doc = {}
+    for server, home, d, q0, qlen, kvlen, pairs in tasks:
+        assert 0 <= server < k and 0 <= home < k and kvlen == q0 + qlen and qlen >= 1
+        assert pairs == O.pairs_of_range(q0, q0 + qlen)
+        per_doc.setdefault(d, []).append((q0, q0 + qlen))
+    for d, L in enumerate(docs):
+        segs = sorted(per_doc[d])
+        assert segs[0][0] == 0 and segs[-1][1] == L
+        assert all(a[1] == b[0] for a, b in zip(segs, segs[1:]))
+    total = sum(L * (L + 1) // 2 for L in docs)
+    assert sum(t[6] for t in tasks) == total
+    loads = [0] * k
+    for t in tasks:
+        loads[t[0]] += t[6]
+    assert loads == st["loads"]
+    target = total / k
+    assert min(loads) >= target * (1 - eps) - 1e-9
+    # the shards started on the device that held their tokens
+    T = -(-sum(docs) // k)
+    offs = np.concatenate([[0], np.cumsum(docs)[:-1]])
+    for server, home, d, q0, qlen, kvlen, pairs in tasks:
+        assert min((offs[d] + q0) // T, k - 1) == home
+
+
+# ---------------------------------------------------------------- the library against the oracle
+
+def test_library_optimal_shard_equals_oracle():
+    rng = np.random.default_rng(3)
+    for _ in range(2000):
+        L_kv = int(rng.integers(1, 300000))
+        L_q = int(rng.integers(1, L_kv + 1))
+        alpha = float(rng.uniform(1e-4, 1.0))
+        f = L_q * L_kv - L_q * (L_q - 1) // 2
+        tgt = max(1, int(math.floor(alpha * f + 0.5)))
+        bq, bkv = float(rng.uniform(0.5, 8.0)), float(rng.uniform(0.1, 8.0))
+        got = capi.optimal_shard(L_q, L_kv, alpha, tgt, bq, bkv)
+        if L_kv - L_q > 20000:
+            # oracle's brute-force context search over a very wide range is slow; compare via the closed form
+            n_real, _, _ = O.optimal_shard_real(L_q, L_kv, alpha, bq, bkv)
+            assert got[2] == pytest.approx(n_real, rel=1e-12, abs=1e-12)
+            continue
+        exp = O.optimal_shard(L_q, L_kv, alpha, tgt, bq, bkv)
+        assert got[:2] == exp[:2]
+        assert got[2] == pytest.approx(exp[2], rel=1e-12, abs=1e-12)
+
+
+def test_library_profile_equals_oracle():
+    nq, nkv, sec, _ = bilinear_grid()
+    sec = [[s * (1.0 + 0.1 * ((i * 7 + j * 3) % 5)) for j, s in enumerate(row)] for i, row in enumerate(sec)]
+    fpp = 12.0 * 128 * 32
+    prof = capi.Profile(nq, nkv, sec, fpp)
+    assert prof.peak() == pytest.approx(O.profile_peak(nq, nkv, sec, fpp), rel=1e-14)
+    rng = np.random.default_rng(4)
+    for _ in range(1000):
+        y = int(rng.integers(1, 200000))
+        x = int(rng.integers(1, y + 1))
+        assert prof.predict(x, y) == pytest.approx(O.profile_predict(nq, nkv, sec, fpp, x, y), rel=1e-13)
+    prof.close()
+
+
+@pytest.mark.parametrize("name", list(doc_sets()))
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_library_schedule_equals_oracle(name, k):
+    docs = doc_sets()[name]
+    for eps, min_shard in [(0.0, 0), (0.02, 128)]:
+        got, res = capi.schedule(docs, k, 8192.0, 4096.0, tolerance=eps, min_shard_tokens=min_shard)
+        exp, st = O.schedule(docs, k, 8192.0, 4096.0, tolerance=eps, min_shard_tokens=min_shard)
+        assert as_tuples(got) == [tuple(t) for t in exp]
+        assert res["n_migrations"] == st["n_migrations"] and res["n_splits"] == st["n_splits"]
+        assert res["comm_bytes"] == st["comm_bytes"]
+        assert res["max_load"] == st["max_load"] and res["min_load"] == st["min_load"]
+
+
+def test_library_rejects_bad_arguments():
+    with pytest.raises(capi.CAError):
+        capi.schedule([], 2, 1.0, 1.0)
+    with pytest.raises(capi.CAError):
+        capi.schedule([10, 0], 2, 1.0, 1.0)
+    with pytest.raises(capi.CAError):
+        capi.schedule([10], 0, 1.0, 1.0)
+    with pytest.raises(capi.CAError):
+        capi.optimal_shard(10, 5, 0.5, 3, 1.0, 1.0)
+    with pytest.raises(capi.CAError):
+        capi.optimal_shard(5, 10, 0.0, 3, 1.0, 1.0)
+    with pytest.raises(capi.CAError):
+        capi.Profile([128, 64], [128], [[1.0], [1.0]], 1.0)
+    with pytest.raises(capi.CAError):
+        capi.Profile([128], [128], [[0.0]], 1.0)
+
+
+# ---------------------------------------------------------------- two servers as gloo ranks
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank(rank, world, port, docs, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    from document_masked_core_gb300 import capi as C
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    tasks, _ = C.schedule(docs, world, 8192.0, 4096.0, tolerance=0.01)
+    mine = [(int(t["doc_id"]), int(t["q_start"]), int(t["q_len"])) for t in tasks if t["server"] == rank]
+    flat = torch.tensor([x for m in mine for x in m] or [0], dtype=torch.int64)
+    n = torch.tensor([len(mine)], dtype=torch.int64)
+    ns = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(ns, n)
+    width = int(max(x.item() for x in ns)) * 3 or 1
+    pad = torch.zeros(width, dtype=torch.int64)
+    pad[: flat.numel()] = flat if len(mine) else pad[:0]
+    bufs = [torch.zeros(width, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(bufs, pad)
+    # each rank checks that the union of everyone's share covers every token once
+    covered = {}
+    for r in range(world):
+        vals = bufs[r][: int(ns[r].item()) * 3].tolist()
+        for i in range(0, len(vals), 3):
+            d, q0, ql = vals[i:i + 3]
+            covered.setdefault(d, []).append((q0, q0 + ql))
+    ok = True
+    for d, L in enumerate(docs):
+        segs = sorted(covered.get(d, []))
+        ok &= bool(segs) and segs[0][0] == 0 and segs[-1][1] == L and all(a[1] == b[0] for a, b in zip(segs, segs[1:]))
+    out[rank] = (ok, len(mine), sum(t["pairs"] for t in tasks if t["server"] == rank))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_share_one_schedule():
+    docs = doc_sets()["llama8b_64k"]
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_rank, args=(2, port, docs, out), nprocs=2, start_method="spawn")
+        res = dict(out)
+    assert res[0][0] and res[1][0]
+    total = sum(L * (L + 1) // 2 for L in docs)
+    assert res[0][2] + res[1][2] == total
+    assert abs(res[0][2] - res[1][2]) <= 0.02 * total / 2
