@@ -32,7 +32,7 @@ EXPORTS = [
     "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
     "ca_profile_create", "ca_profile_predict", "ca_profile_peak", "ca_profile_destroy", "ca_optimal_shard",
-    "ca_schedule",
+    "ca_schedule", "ca_shard_2n",
 ]
 
 
@@ -141,6 +141,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_optimal_shard.restype = st
     L.ca_optimal_shard.argtypes = [i64, i64, dbl, i64, dbl, dbl, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                    ctypes.POINTER(dbl)]
+    L.ca_shard_2n.restype = st
+    L.ca_shard_2n.argtypes = [vp, i32, i32, ctypes.POINTER(SchedTask), i64, ctypes.POINTER(i64)]
     L.ca_schedule.restype = st
     L.ca_schedule.argtypes = [vp, i32, ctypes.POINTER(SchedParams), ctypes.POINTER(SchedTask), i64,
                               ctypes.POINTER(SchedResult)]
@@ -376,8 +378,23 @@ def schedule(doc_len, n_servers: int, bytes_q: float, bytes_kv: float, tolerance
             cap = int(res.n_tasks)
             continue
         _check(st)
-    n = int(res.n_tasks)
-    dt = np.dtype([("server", np.int32), ("home", np.int32), ("doc_id", np.int32), ("reserved", np.int32),
-                   ("q_start", np.int64), ("q_len", np.int64), ("kv_len", np.int64), ("pairs", np.int64)])
-    tasks = np.frombuffer(bytes(buf)[: n * ctypes.sizeof(SchedTask)], dtype=dt).copy()
-    return tasks, res.as_dict()
+    return _sched_tasks(buf, int(res.n_tasks)), res.as_dict()
+
+
+_SCHED_DTYPE = np.dtype([("server", np.int32), ("home", np.int32), ("doc_id", np.int32), ("reserved", np.int32),
+                         ("q_start", np.int64), ("q_len", np.int64), ("kv_len", np.int64), ("pairs", np.int64)])
+
+
+def _sched_tasks(buf, n):
+    return np.frombuffer(bytes(buf)[: n * ctypes.sizeof(SchedTask)], dtype=_SCHED_DTYPE).copy()
+
+
+def shard_2n(doc_len, n_ranks: int):
+    """ca_shard_2n: 2N-chunk load-balanced shards of every document."""
+    L = load()
+    dl = np.ascontiguousarray(doc_len, dtype=np.int64)
+    n = ctypes.c_int64()
+    cap = 2 * len(dl) * int(n_ranks)
+    buf = (SchedTask * max(cap, 1))()
+    _check(L.ca_shard_2n(dl.ctypes.data, len(dl), int(n_ranks), buf, cap, ctypes.byref(n)))
+    return _sched_tasks(buf, int(n.value))

@@ -294,3 +294,38 @@ extern "C" ca_status_t ca_schedule(const int64_t *doc_len, int32_t n_docs, const
     }
     return CA_OK;
 }
+
+extern "C" ca_status_t ca_shard_2n(const int64_t *doc_len, int32_t n_docs, int32_t n_ranks, ca_sched_task_t *tasks_out,
+                                   int64_t max_tasks, int64_t *n_tasks_out) {
+    using ca::fail;
+    if (!doc_len || !n_tasks_out || n_docs < 1) return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: NULL or empty input");
+    if (n_ranks < 1) return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: n_ranks must be >= 1");
+    for (int32_t d = 0; d < n_docs; ++d)
+        if (doc_len[d] < 1 || doc_len[d] > (int64_t(1) << 31))
+            return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: document " + std::to_string(d) + " has an invalid length");
+    std::vector<ca_sched_task_t> out;
+    const int64_t two_n = 2 * static_cast<int64_t>(n_ranks);
+    for (int32_t r = 0; r < n_ranks; ++r)
+        for (int32_t d = 0; d < n_docs; ++d) {
+            const int64_t L = doc_len[d], c = (L + two_n - 1) / two_n;
+            const int64_t chunks[2] = {r, two_n - 1 - r};
+            for (int64_t j : chunks) {  // ascending q_start: j = r first, then 2N-1-r
+                const int64_t a = j * c, b = std::min((j + 1) * c, L);
+                if (a >= b) continue;
+                ca_sched_task_t t{};
+                t.server = r;
+                t.home = r;
+                t.doc_id = d;
+                t.q_start = a;
+                t.q_len = b - a;
+                t.kv_len = b;
+                t.pairs = range_pairs(a, b);
+                out.push_back(t);
+            }
+        }
+    *n_tasks_out = static_cast<int64_t>(out.size());
+    if (!tasks_out || max_tasks < *n_tasks_out)
+        return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: task buffer too small (" + std::to_string(*n_tasks_out) + " needed)");
+    std::copy(out.begin(), out.end(), tasks_out);
+    return CA_OK;
+}

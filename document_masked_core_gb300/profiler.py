@@ -121,15 +121,82 @@ def report(grid: dict, doc_sets: dict, servers=(2, 4, 8), hq=32, hkv=8, d=128, r
     return rows
 
 
+SHARD_LENGTHS = [8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096]
+
+
+def sweep_shard_lengths(lengths=SHARD_LENGTHS, total_q=32768, n_docs=16, doc_len=32768, hq=32, hkv=8, d=128,
+                        reps=5, warmup=2, seed=0):
+    """Throughput of one rebatched launch of total_q query tokens made of shards
+    of one length s, each placed at a uniformly random position of one of
+    n_docs documents of doc_len tokens (so contexts vary from s to doc_len),
+    for every s (the composability measurement of "Efficient Long-context
+    Language Model Training by Core Attention Disaggregation", "Property 2:
+    Composability", Figure 5).  TFLOP/s over 12*d*H_q*causal pairs."""
+    rng = np.random.default_rng(seed)
+    docs = np.full(n_docs, doc_len, dtype=np.int64)
+    rows = []
+    for s in lengths:
+        m = total_q // s
+        tasks = []
+        for t in range(m):
+            q0 = int(rng.integers(0, doc_len - s + 1))
+            tasks.append((t % n_docs, q0, s, 0, q0 + s))
+        pairs = sum(s * (q0 + s) - s * (s - 1) // 2 for _, q0, _, _, _ in tasks)
+        sec = _launch_time(docs, tasks, hq, hkv, d, reps, warmup)
+        rows.append({"shard_tokens": s, "shards": m, "causal_pairs": pairs, "fwd_bwd_ms": sec * 1e3,
+                     "tflops": 12.0 * d * hq * pairs / sec / 1e12})
+    return rows
+
+
+def rank_balance(doc_sets: dict, ranks=(2, 4, 8)):
+    """Max / mean causal pairs per rank: contiguous token ranges of the whole
+    chunk vs the 2N-chunk shards of every document."""
+    out = []
+    for name, docs in doc_sets.items():
+        docs = [int(x) for x in docs]
+        total = sum(docs)
+        for n in ranks:
+            T = -(-total // n)
+            cont = [0] * n
+            off = 0
+            for L in docs:
+                pos = off
+                while pos < off + L:
+                    r = min(pos // T, n - 1)
+                    stop = min(off + L, (r + 1) * T)
+                    a, b = pos - off, stop - off
+                    cont[r] += b * (b + 1) // 2 - a * (a + 1) // 2
+                    pos = stop
+                off += L
+            two = [0] * n
+            for t in capi.shard_2n(docs, n):
+                two[int(t["server"])] += int(t["pairs"])
+            out.append({"docs": name, "ranks": n, "contiguous": max(cont) / (sum(cont) / n),
+                        "two_n_chunk": max(two) / (sum(two) / n)})
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
-    ap.add_argument("--out", required=True, help="grid JSON to write (or read with --report-only)")
+    ap.add_argument("--out", help="grid JSON to write (or read with --report-only)")
     ap.add_argument("--hq", type=int, default=32)
     ap.add_argument("--hkv", type=int, default=8)
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--report", help="also schedule the bench's document sets and write this JSON")
     ap.add_argument("--report-only", action="store_true", help="read the grid from --out instead of measuring")
+    ap.add_argument("--sweep", help="measure throughput vs shard length and write this JSON (no grid)")
     a = ap.parse_args(argv)
+    if a.sweep:
+        import workloads as W
+        rows = sweep_shard_lengths(hq=a.hq, hkv=a.hkv, d=a.head_dim)
+        bal = rank_balance({"llama8b_chunk_64k": W.llama8b_chunk(seed=0).doc_len,
+                            "pool_16_docs": W.rebatched_pool().doc_len,
+                            "long_chunk_512k": W.long_context_chunk().doc_len})
+        with open(a.sweep, "w") as f:
+            json.dump({"sweep": rows, "rank_balance": bal}, f, indent=1)
+        for r in rows + bal:
+            print(json.dumps({k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}))
+        return
     if a.report_only:
         with open(a.out) as f:
             grid = json.load(f)

@@ -156,6 +156,25 @@ typedef struct {
 ca_status_t ca_schedule(const int64_t *doc_len, int32_t n_docs, const ca_sched_params_t *params,
                         ca_sched_task_t *tasks_out, int64_t max_tasks, ca_sched_result_t *result);
 
+/* ------------------------------------------------------------------ 2N-chunk sharding */
+
+/*
+ * Load-balanced sharding of every document over n_ranks ranks ("Context
+ * Parallelism for Scalable Million-Token Inference", §3.5.1 "Load-Balanced
+ * Sharding of Input Sequences"; the head-tail shards of "Efficient
+ * Long-context Language Model Training by Core Attention Disaggregation",
+ * "The role of head-tail sharding in practice"): each document is cut into
+ * 2N chunks C_0 .. C_{2N-1} and rank i takes C_i and C_{2N-1-i}.  Padding is
+ * not materialised: chunk size c = ceil(L / 2N), chunk j covers positions
+ * [j c, min((j+1) c, L)), and empty chunks are omitted.  Each chunk becomes
+ * one CA-task with its prefix context (server = home = rank).  Tasks are
+ * written grouped by rank, then by (doc_id, q_start); *n_tasks_out receives
+ * the count (also when max_tasks is too small, which returns
+ * CA_ERR_INVALID_ARG).
+ */
+ca_status_t ca_shard_2n(const int64_t *doc_len, int32_t n_docs, int32_t n_ranks, ca_sched_task_t *tasks_out,
+                        int64_t max_tasks, int64_t *n_tasks_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,9 @@ Disaggregation":
     form and its boundary rule; then the integer shard.
   * ``schedule``         -- "The Communication-Aware Greedy Scheduler", steps
     1 to 4, in the order the section gives them.
+  * ``shard_2n``         -- "Context Parallelism for Scalable Million-Token
+    Inference", §3.5.1: 2N chunks per sequence, rank i takes C_i and
+    C_{2N-i-1} (padding not materialised: the last chunks are shorter).
 
 Readings where the pages leave a step open (the same ones the library states
 in include/ca_sched.h): work is counted in exact causal pairs; devices hold
@@ -190,3 +193,19 @@ def schedule(doc_len, k, bytes_q, bytes_kv, tolerance=0.0, min_score=0.0, min_sh
               pairs_of_range(it["q0"], it["q1"])) for it in live]
     stats.update({"max_load": max(load), "min_load": min(load), "target": target, "loads": load})
     return tasks, stats
+
+
+# ---------------------------------------------------------------- 2N-chunk sharding
+
+def shard_2n(doc_len, N):
+    """(rank, rank, doc, q_start, q_len, kv_len, pairs) for every non-empty chunk."""
+    out = []
+    for r in range(N):
+        for d, L in enumerate(doc_len):
+            c = -(-L // (2 * N))
+            chunks = [[p for p in range(L) if p // c == j] for j in range(2 * N)]  # positions of chunk j
+            for j in sorted({r, 2 * N - 1 - r}):
+                pos = chunks[j]
+                if pos:
+                    out.append((r, r, d, pos[0], len(pos), pos[-1] + 1, pairs_of_range(pos[0], pos[-1] + 1)))
+    return out

@@ -245,6 +245,55 @@ def test_library_rejects_bad_arguments():
         capi.Profile([128], [128], [[0.0]], 1.0)
 
 
+# ---------------------------------------------------------------- 2N-chunk sharding
+
+def test_shard_2n_matches_the_pages_example():
+    path = os.path.join(ROOT, "tests", "golden", "shard_2n_example.txt")
+    N, expect = None, {}
+    for line in open(path):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "N":
+            N = int(f[1])
+        elif f[0] == "rank":
+            expect[int(f[1])] = (int(f[2]), int(f[3]))
+    L = 2 * N * 5  # chunk size 5
+    for r, (a, b) in expect.items():
+        got = [(t[3], t[4]) for t in O.shard_2n([L], N) if t[0] == r]
+        assert got == [(5 * a, 5), (5 * b, 5)]
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8])
+def test_shard_2n_balances_exactly_when_divisible(N):
+    """Chunk j of size c holds c*(j c) + c(c+1)/2 pairs; chunks j and 2N-1-j
+    together hold c^2 (2N-1) + c(c+1), the same for every rank."""
+    for c in (1, 3, 16, 128):
+        L = 2 * N * c
+        per = [0] * N
+        for r, _, d, q0, ql, kvl, pairs in O.shard_2n([L], N):
+            assert pairs == sum(p + 1 for p in range(q0, q0 + ql))
+            per[r] += pairs
+        assert per == [c * c * (2 * N - 1) + c * (c + 1)] * N
+
+
+def test_shard_2n_covers_every_token_once_and_library_agrees():
+    rng = np.random.default_rng(5)
+    for _ in range(40):
+        docs = [int(x) for x in rng.integers(1, 3000, int(rng.integers(1, 12)))]
+        N = int(rng.integers(1, 9))
+        exp = O.shard_2n(docs, N)
+        got = capi.shard_2n(docs, N)
+        assert as_tuples(got) == [tuple(t) for t in exp]
+        cover = {}
+        for r, _, d, q0, ql, kvl, pairs in exp:
+            assert kvl == q0 + ql
+            cover.setdefault(d, []).append((q0, q0 + ql))
+        for d, L in enumerate(docs):
+            segs = sorted(cover[d])
+            assert segs[0][0] == 0 and segs[-1][1] == L and all(a[1] == b[0] for a, b in zip(segs, segs[1:]))
+
+
 # ---------------------------------------------------------------- two servers as gloo ranks
 
 def _free_port():

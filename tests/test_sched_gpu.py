@@ -1,5 +1,6 @@
-"""The scheduler's shards run on simulated attention servers (one after
-another on this GPU): per server one rebatched launch of its CA-tasks, query
+"""The scheduler's shards and the 2N-chunk shards run on simulated attention
+servers / ranks (one after another on this GPU): per server one rebatched
+launch of its CA-tasks, query
 rows gathered from the devices that hold them.  The forward rows equal the
 one-task-per-document launch bit for bit (key tiles sit at document
 coordinates); dQ rows and the dK / dV partials summed over servers match it
@@ -41,24 +42,21 @@ def run_plan(w, q, k, v, do, o_dtype):
     return o, lse, dq, dk, dv
 
 
-@pytest.mark.parametrize("k,min_shard", [(4, 0), (3, 128)])
-def test_scheduled_servers_equal_unsharded(k, min_shard):
-    docs = W.llama8b_chunk(seed=2, total=16384).doc_len
-    hq, hkv, d = 32, 8, 128
-    tasks, res = capi.schedule(docs, k, hq * d * 2.0, 2 * hkv * d * 2.0, tolerance=0.01,
-                               min_shard_tokens=min_shard)
+def check_servers(docs, tasks, k, hq=32, hkv=8, d=128, seed=9):
+    """Run every server's tasks as one launch and compare with the
+    one-task-per-document launch."""
     whole = W.custom("whole", docs, [(i, 0, int(L), 0, int(L)) for i, L in enumerate(docs)], hq=hq, hkv=hkv, d=d,
-                     seed=9)
+                     seed=seed)
     q, kk, v, do = W.make_tensors(whole, device="cuda")
-    ow, lw, dqw, dkw, dvw = run_plan(whole, q, kk, v, do, ca.CA_DTYPE_FP32)
-    ow16, lw16, dqw16, dkw16, dvw16 = run_plan(whole, q, kk, v, do, ca.CA_DTYPE_BF16)
-    dk_sum = torch.zeros_like(dkw, dtype=torch.float32)
-    dv_sum = torch.zeros_like(dvw, dtype=torch.float32)
+    ow, lw, _, _, _ = run_plan(whole, q, kk, v, do, ca.CA_DTYPE_FP32)
+    _, _, dqw16, dkw16, dvw16 = run_plan(whole, q, kk, v, do, ca.CA_DTYPE_BF16)
+    dk_sum = torch.zeros_like(dkw16, dtype=torch.float32)
+    dv_sum = torch.zeros_like(dvw16, dtype=torch.float32)
     for s in range(k):
         mine = [t for t in tasks if t["server"] == s]
         assert mine, "every server gets work"
         ws_ = W.custom(f"server{s}", docs, [(int(t["doc_id"]), int(t["q_start"]), int(t["q_len"]), 0,
-                                              int(t["kv_len"])) for t in mine], hq=hq, hkv=hkv, d=d, seed=9)
+                                              int(t["kv_len"])) for t in mine], hq=hq, hkv=hkv, d=d, seed=seed)
         rows = torch.as_tensor(np.concatenate([int(whole.doc_kv_offset[int(t["doc_id"])]) +
                                                np.arange(int(t["q_start"]), int(t["q_start"] + t["q_len"]))
                                                for t in mine]), device="cuda")
@@ -71,6 +69,19 @@ def test_scheduled_servers_equal_unsharded(k, min_shard):
         dv_sum += dvs.float()
     assert rfro(dk_sum, dkw16) <= GRAD_RFRO / 4
     assert rfro(dv_sum, dvw16) <= GRAD_RFRO / 4
+
+
+@pytest.mark.parametrize("k,min_shard", [(4, 0), (3, 128)])
+def test_scheduled_servers_equal_unsharded(k, min_shard):
+    docs = W.llama8b_chunk(seed=2, total=16384).doc_len
+    tasks, _ = capi.schedule(docs, k, 32 * 128 * 2.0, 2 * 8 * 128 * 2.0, tolerance=0.01, min_shard_tokens=min_shard)
+    check_servers(docs, tasks, k)
+
+
+@pytest.mark.parametrize("n_ranks", [2, 4])
+def test_2n_chunk_ranks_equal_unsharded(n_ranks):
+    docs = W.llama8b_chunk(seed=4, total=16384).doc_len
+    check_servers(docs, capi.shard_2n(docs, n_ranks), n_ranks)
 
 
 def test_cost_model_from_a_measured_grid():
