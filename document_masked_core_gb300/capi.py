@@ -28,7 +28,8 @@ CA_DTYPE_FP32 = 1
 
 # names declared in include/ca.h and include/ca_sched.h, in order
 EXPORTS = [
-    "ca_plan_create", "ca_plan_dry_run", "ca_plan_info", "ca_plan_task_pairs", "ca_plan_destroy",
+    "ca_plan_create", "ca_plan_dry_run", "ca_plan_create_masked", "ca_plan_dry_run_masked", "ca_plan_info",
+    "ca_plan_task_pairs", "ca_plan_destroy",
     "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
     "ca_profile_create", "ca_profile_predict", "ca_profile_peak", "ca_profile_destroy", "ca_optimal_shard",
@@ -45,6 +46,10 @@ class CAError(RuntimeError):
 class Task(ctypes.Structure):
     _fields_ = [("doc_id", ctypes.c_int32), ("reserved", ctypes.c_int32), ("q_start", ctypes.c_int64),
                 ("q_len", ctypes.c_int64), ("kv_start", ctypes.c_int64), ("kv_len", ctypes.c_int64)]
+
+
+class Mask(ctypes.Structure):
+    _fields_ = [("sink", ctypes.c_int64), ("lo", ctypes.c_int64), ("window", ctypes.c_int64)]
 
 
 class Shape(ctypes.Structure):
@@ -101,6 +106,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_plan_dry_run.restype = st
     L.ca_plan_dry_run.argtypes = [ctypes.POINTER(Task), i32, vp, vp, i32, ctypes.POINTER(Shape),
                                   ctypes.POINTER(PlanInfo), vp]
+    L.ca_plan_create_masked.restype = st
+    L.ca_plan_create_masked.argtypes = [ctypes.POINTER(Task), vp, i32, vp, vp, i32, ctypes.POINTER(Shape), vp,
+                                        ctypes.POINTER(vp)]
+    L.ca_plan_dry_run_masked.restype = st
+    L.ca_plan_dry_run_masked.argtypes = [ctypes.POINTER(Task), vp, i32, vp, vp, i32, ctypes.POINTER(Shape),
+                                         ctypes.POINTER(PlanInfo), vp]
     L.ca_plan_info.restype = st
     L.ca_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.ca_plan_task_pairs.restype = st
@@ -187,13 +198,33 @@ def _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len):
     return arr, n
 
 
+def _mask_array(masks, n):
+    """(sink, lo, window) triples (or None) -> ca_mask_t array (or None)."""
+    if masks is None:
+        return None
+    m = np.asarray(masks, dtype=np.int64).reshape(-1, 3)
+    if len(m) != n:
+        raise ValueError("one mask per task")
+    if not m.any():
+        return None
+    arr = (Mask * n)()
+    for i in range(n):
+        arr[i].sink, arr[i].lo, arr[i].window = (int(x) for x in m[i])
+    return arr
+
+
+def _workload_masks(w):
+    return np.stack(w.masks(), axis=1) if getattr(w, "masked", False) else None
+
+
 def dry_run(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len, doc_len, doc_kv_offset,
             num_q_heads: int, num_kv_heads: int, head_dim: int, softmax_scale: Optional[float] = None,
-            o_dtype: int = CA_DTYPE_BF16):
-    """ca_plan_dry_run: validation and integer accounting without a device.
-    Returns (info dict, per-task pairs)."""
+            o_dtype: int = CA_DTYPE_BF16, masks=None):
+    """ca_plan_dry_run(_masked): validation and integer accounting without a
+    device.  Returns (info dict, per-task pairs)."""
     L = load()
     arr, n = _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len)
+    marr = _mask_array(masks, n)
     dl = np.ascontiguousarray(doc_len, dtype=np.int64)
     do = np.ascontiguousarray(doc_kv_offset, dtype=np.int64)
     if softmax_scale is None:
@@ -201,14 +232,15 @@ def dry_run(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len, doc_
     shape = Shape(num_q_heads, num_kv_heads, head_dim, float(softmax_scale), int(o_dtype))
     info = PlanInfo()
     pairs = np.zeros(max(n, 1), dtype=np.int64)
-    _check(L.ca_plan_dry_run(arr, n, dl.ctypes.data, do.ctypes.data, len(dl), ctypes.byref(shape),
-                             ctypes.byref(info), pairs.ctypes.data))
+    _check(L.ca_plan_dry_run_masked(arr, marr, n, dl.ctypes.data, do.ctypes.data, len(dl), ctypes.byref(shape),
+                                    ctypes.byref(info), pairs.ctypes.data))
     return info.as_dict(), pairs[:n]
 
 
 def dry_run_workload(w):
     return dry_run(w.task_doc, w.task_q_start, w.task_q_len, w.task_kv_start, w.task_kv_len, w.doc_len,
-                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale)
+                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale,
+                   masks=_workload_masks(w))
 
 
 class Plan:
@@ -216,17 +248,18 @@ class Plan:
 
     def __init__(self, task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len, doc_len, doc_kv_offset,
                  num_q_heads: int, num_kv_heads: int, head_dim: int, softmax_scale: Optional[float] = None,
-                 o_dtype: int = CA_DTYPE_BF16, stream=None):
+                 o_dtype: int = CA_DTYPE_BF16, stream=None, masks=None):
         L = load()
         arr, n = _task_array(task_doc, task_q_start, task_q_len, task_kv_start, task_kv_len)
+        marr = _mask_array(masks, n)
         self._doc_len = np.ascontiguousarray(doc_len, dtype=np.int64)
         self._doc_off = np.ascontiguousarray(doc_kv_offset, dtype=np.int64)
         if softmax_scale is None:
             softmax_scale = head_dim ** -0.5
         shape = Shape(num_q_heads, num_kv_heads, head_dim, float(softmax_scale), int(o_dtype))
         h = ctypes.c_void_p()
-        _check(L.ca_plan_create(arr, n, self._doc_len.ctypes.data, self._doc_off.ctypes.data,
-                                len(self._doc_len), ctypes.byref(shape), _stream(stream), ctypes.byref(h)))
+        _check(L.ca_plan_create_masked(arr, marr, n, self._doc_len.ctypes.data, self._doc_off.ctypes.data,
+                                       len(self._doc_len), ctypes.byref(shape), _stream(stream), ctypes.byref(h)))
         self._h = h
         self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
         self.o_dtype = o_dtype
@@ -235,7 +268,8 @@ class Plan:
     @classmethod
     def from_workload(cls, w, o_dtype: int = CA_DTYPE_BF16, stream=None) -> "Plan":
         return cls(w.task_doc, w.task_q_start, w.task_q_len, w.task_kv_start, w.task_kv_len, w.doc_len,
-                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale, o_dtype, stream)
+                   w.doc_kv_offset, w.num_q_heads, w.num_kv_heads, w.head_dim, w.softmax_scale, o_dtype, stream,
+                   masks=_workload_masks(w))
 
     @property
     def handle(self) -> int:

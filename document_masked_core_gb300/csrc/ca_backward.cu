@@ -204,17 +204,18 @@ __device__ __forceinline__ KvGeo decode_kv(const BwdParams &p, int32_t idx) {
     return k;
 }
 
-// Query tiles of task t that see key tile jt (same rule as the host plan).
+// Query tiles of task t that see key tile jt (same rule as the host plan):
+// the rows of key_tile_rows inside the task.
 __device__ __forceinline__ void task_tiles(const DevTask &t, int32_t jt, int32_t tpt, int32_t &first, int32_t &count) {
-    const int32_t k0 = jt * kTileKeys, k1 = k0 + kTileKeys;
-    const int32_t a = t.kv_start, e = t.kv_start + t.kv_len;
     first = 0;
     count = 0;
-    if (k1 <= a || k0 >= e) return;
-    const int32_t pmin = max(k0, a);
-    if (pmin >= t.q_start + t.q_len) return;
-    first = (max(pmin, t.q_start) - t.q_start) / tpt;
-    count = (t.q_len - 1) / tpt - first + 1;
+    int32_t pmin, pmax;
+    key_tile_rows(t, jt * kTileKeys, &pmin, &pmax);
+    const int32_t q0 = t.q_start, q1 = t.q_start + t.q_len - 1;
+    const int32_t lo = max(pmin, q0), hi = min(pmax, q1);
+    if (lo > hi) return;
+    first = (lo - q0) / tpt;
+    count = (hi - q0) / tpt - first + 1;
 }
 
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
@@ -673,7 +674,11 @@ __global__ void __launch_bounds__(512, 1)
                 const DevTask t = p.tasks[p.doc_tasks[k]];
                 int32_t first, count;
                 task_tiles(t, kg.jt, p.tpt, first, count);
-                const bool key_in_block = kpos >= t.kv_start && kpos < t.kv_start + t.kv_len;
+                // rows that see this key: [kpos, row_end] (sink key: unbounded; window:
+                // kpos + win - 1), none when the key is outside the block or below lo
+                const bool key_in_block = kpos >= t.kv_start && kpos < t.kv_start + t.kv_len &&
+                                          (kpos < t.sink || kpos >= t.lo);
+                const int64_t row_end = (kpos < t.sink || t.win == 0) ? int64_t(1) << 40 : int64_t(kpos) + t.win - 1;
                 for (int32_t tile = first; tile < first + count; ++tile, ++qt) {
                     const int32_t tok0 = tile * p.tpt;
                     const int32_t ntok = min(p.tpt, t.q_len - tok0);
@@ -683,9 +688,11 @@ __global__ void __launch_bounds__(512, 1)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.row_full[qt & 1], (qt >> 1) & 1, wd));
                     if (!ok) break;
                     // visible rows for this key: tile rows r (token r / G) with
-                    // r_lo <= r < r_hi, i.e. p >= key position and the token inside the task
-                    const int32_t r_hi = ntok * p.G;
-                    const int32_t r_lo = key_in_block ? max(kpos - p_first, 0) * p.G : r_hi;
+                    // r_lo <= r < r_hi, i.e. kpos <= p <= row_end and the token inside the task
+                    const int32_t tok_hi = static_cast<int32_t>(
+                        row_end - p_first + 1 < ntok ? (row_end - p_first + 1 > 0 ? row_end - p_first + 1 : 0) : ntok);
+                    const int32_t r_hi = tok_hi * p.G;
+                    const int32_t r_lo = key_in_block ? min(max(kpos - p_first, 0) * p.G, r_hi) : r_hi;
                     const bool edge = r_lo > c0 || r_hi < c0 + 64;
                     // ---- P'^T = scale P^T = exp2(scale log2(e) S^T - log2(e) LSE + log2(scale))
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, qt & 1, wd));

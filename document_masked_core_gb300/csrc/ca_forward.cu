@@ -95,8 +95,13 @@ struct TileGeo {
     int32_t row0, p_first, ntok, n_kv;  // n_kv = 0: tile absent or sees nothing
 };
 
+// Key tiles of an item: the sequence of key_tile_ranges over the rows of its
+// two query tiles; tile x visits the prefix of n_kv(x) entries that reaches
+// its last row's last visible key (the same rule as the host plan).
 struct ItemGeo {
-    int32_t g, kv_start, kv_end, kv_off, j_first, n_kv;
+    int32_t g, kv_off, n_kv;
+    KeyTileRanges kr;
+    DevTask task;
     TileGeo t[2];
 };
 
@@ -105,28 +110,25 @@ __device__ __forceinline__ TileGeo tile_geo(const DevTask &t, int32_t tile, int3
     const int32_t tok0 = tile * tpt;
     tg.row0 = t.row0 + tok0;
     tg.p_first = t.q_start + tok0;
-    tg.ntok = min(tpt, t.q_len - tok0);
-    if (tg.ntok <= 0) {
-        tg.ntok = 0;
-        tg.n_kv = 0;
-        return tg;
-    }
-    const int32_t hi = min(t.kv_start + t.kv_len, tg.p_first + tg.ntok);  // exclusive
-    tg.n_kv = hi <= t.kv_start ? 0 : (hi - 1) / kTileKeys - t.kv_start / kTileKeys + 1;
+    tg.ntok = max(0, min(tpt, t.q_len - tok0));
+    tg.n_kv = 0;
     return tg;
 }
 
 __device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) {
     const FwdItem it = p.items[idx];
-    const DevTask t = p.tasks[it.task];
     ItemGeo gi;
+    gi.task = p.tasks[it.task];
+    const DevTask &t = gi.task;
     gi.g = it.g;
-    gi.kv_start = t.kv_start;
-    gi.kv_end = t.kv_start + t.kv_len;
     gi.kv_off = t.kv_off;
-    gi.j_first = t.kv_start / kTileKeys;
     gi.t[0] = tile_geo(t, it.tile, p.tpt);
     gi.t[1] = tile_geo(t, it.tile + 1, p.tpt);
+    const int32_t end0 = gi.t[0].p_first + gi.t[0].ntok - 1;
+    const int32_t end1 = gi.t[1].ntok > 0 ? gi.t[1].p_first + gi.t[1].ntok - 1 : end0;
+    gi.kr = key_tile_ranges(t, gi.t[0].p_first, end1);
+    gi.t[0].n_kv = gi.t[0].ntok > 0 ? visits_upto(gi.kr, t, end0) : 0;
+    gi.t[1].n_kv = gi.t[1].ntok > 0 ? visits_upto(gi.kr, t, end1) : 0;
     gi.n_kv = max(gi.t[0].n_kv, gi.t[1].n_kv);
     return gi;
 }
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(320, 1)
                     const uint32_t st = kv_it % C::kStages;
                     const uint32_t ph = (kv_it / C::kStages) & 1;
                     if (!(ok = mbar_wait(&bars.kv_empty[st], ph ^ 1, wd))) break;
-                    const int32_t key_row = gi.kv_off + (gi.j_first + i) * kTileKeys;
+                    const int32_t key_row = gi.kv_off + gi.kr.tile(i) * kTileKeys;
                     mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
@@ -356,8 +358,7 @@ __global__ void __launch_bounds__(320, 1)
             const int32_t h = gi.g * p.G + (row % p.G);
             const bool valid = tok < tg.ntok;
             const int32_t pos = tg.p_first + min(tok, max(tg.ntok - 1, 0));
-            const int32_t kv_lo = gi.kv_start;
-            const int32_t kv_hi = min(gi.kv_end, pos + 1);
+            const RowKeys rk = row_keys(gi.task, pos);  // visible keys: [a, r1) U [r2, hi)
             const size_t out_idx = static_cast<size_t>(tg.row0 + tok) * p.hq + h;
             if (tg.n_kv == 0) {
                 if (valid) store_row_zero<D, OUT_F32>(p, out_idx);
@@ -375,14 +376,17 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-                const int32_t key0 = (gi.j_first + i) * kTileKeys;
-                if (key0 < kv_lo || key0 + kTileKeys > kv_hi) {
+                const int32_t key0 = gi.kr.tile(i) * kTileKeys;
+                const bool whole = (key0 >= rk.a && key0 + kTileKeys <= rk.r1) ||
+                                   (key0 >= rk.a && key0 >= rk.r2 && key0 + kTileKeys <= rk.hi);
+                if (!whole) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             const int32_t key = key0 + c * 32 + e;
-                            if (key < kv_lo || key >= kv_hi) sr[c][e] = __float_as_uint(-INFINITY);
+                            const bool vis = key >= rk.a && (key < rk.r1 || (key >= rk.r2 && key < rk.hi));
+                            if (!vis) sr[c][e] = __float_as_uint(-INFINITY);
                         }
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY;

@@ -27,7 +27,99 @@ struct DevTask {
     int32_t doc;
     int32_t kv_off;    // first K/V row of the document
     int32_t doc_len;
+    int32_t sink, lo, win;  // sparse visibility (ca_mask_t); 0, 0, 0 = plain
 };
+
+// Visible keys of row p: [kv_start, min(kv_end, p + 1)) intersected with
+// [0, sink) U [max(lo, p - win + 1), inf)  (win = 0: [lo, inf)).  As two
+// intervals [a, r1) U [r2, hi) (either may be empty; they may overlap).
+struct RowKeys {
+    int32_t a, r1, r2, hi;
+};
+
+__host__ __device__ inline RowKeys row_keys(const DevTask &t, int32_t p) {
+    RowKeys k;
+    k.a = t.kv_start;
+    k.hi = p + 1 < t.kv_start + t.kv_len ? p + 1 : t.kv_start + t.kv_len;
+    k.r1 = t.sink < k.hi ? t.sink : k.hi;
+    int32_t lo = t.lo;
+    if (t.win > 0 && p - t.win + 1 > lo) lo = p - t.win + 1;
+    k.r2 = lo > t.kv_start ? lo : t.kv_start;
+    return k;
+}
+
+// Key tiles (of 128) a query tile with rows p in [p0, p1] visits: the sink
+// range [sa, sb) and the window range [wa, wb) of key-tile indices, merged
+// into one range (sb = sa) when they touch or overlap.  Row p0 has the
+// smallest window start and p1 the largest end.
+struct KeyTileRanges {
+    int32_t sa, sb, wa, wb;
+    __host__ __device__ int32_t count() const { return (sb - sa) + (wb - wa); }
+    // key tile of the i-th visit (i < count())
+    __host__ __device__ int32_t tile(int32_t i) const { return i < sb - sa ? sa + i : wa + (i - (sb - sa)); }
+};
+
+__host__ __device__ inline KeyTileRanges key_tile_ranges(const DevTask &t, int32_t p0, int32_t p1) {
+    KeyTileRanges r;
+    const RowKeys k0 = row_keys(t, p0), k1 = row_keys(t, p1);
+    // sink part: keys [a, min(sink, hi(p1)))
+    const int32_t s_end = k1.r1;
+    // window part: keys [r2(p0), hi(p1))
+    const int32_t w_beg = k0.r2, w_end = k1.hi;
+    r.sa = k0.a / 128;
+    r.sb = s_end > k0.a ? (s_end - 1) / 128 + 1 : r.sa;
+    if (w_end > w_beg) {
+        r.wa = w_beg / 128;
+        r.wb = (w_end - 1) / 128 + 1;
+    } else {
+        r.wa = r.wb = 0;
+    }
+    if (r.sb > r.sa && r.wb > r.wa && r.wa <= r.sb) {  // touching or overlapping: one range
+        r.wa = r.sa < r.wa ? r.sa : r.wa;
+        r.wb = r.sb > r.wb ? r.sb : r.wb;
+        r.sb = r.sa;
+    }
+    return r;
+}
+
+// Number of visits (in the order of key_tile_ranges over rows [p0, p1]) up
+// to and including the last key tile row p1x sees: the prefix of the item's
+// sequence a query tile ending at row p1x needs.
+__host__ __device__ inline int32_t visits_upto(const KeyTileRanges &r, const DevTask &t, int32_t p1x) {
+    const RowKeys k = row_keys(t, p1x);
+    int32_t last = -1;  // last visible key of row p1x
+    if (k.hi > k.r2 && k.hi > k.a) last = k.hi - 1;
+    else if (k.r1 > k.a) last = k.r1 - 1;
+    if (last < 0) return 0;
+    const int32_t lt = last / 128;
+    int32_t n = 0;
+    if (lt >= r.sa && r.sb > r.sa) n += (lt < r.sb ? lt + 1 : r.sb) - r.sa;
+    if (r.wb > r.wa && lt >= r.wa) n += (lt < r.wb ? lt + 1 : r.wb) - r.wa;
+    return n;
+}
+
+// Query rows that see at least one key of key tile [k0, k0 + 128): a
+// contiguous range [pmin, pmax] (pmax = INT32_MAX: unbounded); empty when
+// pmin > pmax.  A key j is seen by rows p >= j when j < sink, by rows
+// j <= p <= j + win - 1 when j >= lo (any p >= j when win = 0).
+__host__ __device__ inline void key_tile_rows(const DevTask &t, int32_t k0, int32_t *pmin, int32_t *pmax) {
+    const int32_t j0 = k0 > t.kv_start ? k0 : t.kv_start;
+    const int32_t j1 = (k0 + 128 < t.kv_start + t.kv_len ? k0 + 128 : t.kv_start + t.kv_len) - 1;  // inclusive
+    *pmin = 2147483647;
+    *pmax = -1;
+    if (j1 < j0) return;
+    if (j0 < t.sink) {  // sink keys: every later row
+        *pmin = j0;
+        *pmax = 2147483647;
+    }
+    const int32_t jl = j0 > t.lo ? j0 : t.lo;  // first key past lo
+    if (jl <= j1) {
+        if (jl < *pmin) *pmin = jl;
+        const int64_t hi = t.win > 0 ? static_cast<int64_t>(j1) + t.win - 1 : int64_t(2147483647);
+        const int32_t hi32 = hi < 2147483647 ? static_cast<int32_t>(hi) : 2147483647;
+        if (hi32 > *pmax) *pmax = hi32;
+    }
+}
 
 // Forward item: query tiles `tile` and `tile + 1` (tile even; tokens
 // [tile*T, tile*T+2T) of the task, T = 128 / G) of kv head g, processed

@@ -37,30 +37,33 @@ int64_t task_pairs_closed_form(int64_t q0, int64_t ql, int64_t a, int64_t kl) {
     return total;
 }
 
-// Forward tile geometry, mirrored by the kernel's decode.
-int32_t fwd_tile_nkv(const DevTask &t, int32_t tile, int32_t tpt) {
-    const int32_t tok0 = tile * tpt;
-    const int32_t ntok = std::min(tpt, t.q_len - tok0);
-    const int32_t hi = std::min(t.kv_start + t.kv_len, t.q_start + tok0 + ntok);
-    if (hi <= t.kv_start) return 0;
-    return (hi - 1) / kTileKeys - t.kv_start / kTileKeys + 1;
+// Pairs of a masked task, row by row: |[a, r1) U [r2, hi)| for every row.
+int64_t task_pairs_rows(const DevTask &t) {
+    int64_t total = 0;
+    for (int32_t p = t.q_start; p < t.q_start + t.q_len; ++p) {
+        const RowKeys k = row_keys(t, p);
+        const int64_t c1 = std::max(0, k.r1 - k.a);
+        const int64_t lo2 = std::max(k.r2, k.a);
+        const int64_t c2 = std::max<int64_t>(0, k.hi - lo2);
+        const int64_t ov = std::max<int64_t>(0, std::min<int64_t>(k.r1, k.hi) - lo2);
+        total += c1 + c2 - ov;
+    }
+    return total;
 }
 
-// Query tiles of task t that see key tile jt (mirrored by the backward kernel):
-// rows p >= max(128 jt, kv_start) of the task, provided the key tile
-// intersects the task's block.  Returns the first tile and the count.
+// Query tiles of task t that see key tile jt (mirrored by the backward
+// kernel): the rows of key_tile_rows inside the task.  Returns the first tile
+// and the count.
 void bwd_task_tiles(const DevTask &t, int32_t jt, int32_t tpt, int32_t *first, int32_t *count) {
-    const int32_t k0 = jt * kTileKeys, k1 = k0 + kTileKeys;
-    const int32_t a = t.kv_start, e = t.kv_start + t.kv_len;
     *first = 0;
     *count = 0;
-    if (k1 <= a || k0 >= e) return;
-    const int32_t pmin = std::max(k0, a);
-    const int32_t q1 = t.q_start + t.q_len;
-    if (pmin >= q1) return;
-    const int32_t r = std::max(pmin, t.q_start) - t.q_start;
-    *first = r / tpt;
-    *count = (t.q_len - 1) / tpt - *first + 1;
+    int32_t pmin, pmax;
+    key_tile_rows(t, jt * kTileKeys, &pmin, &pmax);
+    const int32_t q0 = t.q_start, q1 = t.q_start + t.q_len - 1;  // inclusive
+    const int32_t lo = std::max(pmin, q0), hi = std::min(pmax, q1);
+    if (lo > hi) return;
+    *first = (lo - q0) / tpt;
+    *count = (hi - q0) / tpt - *first + 1;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -173,7 +176,7 @@ struct HostPlan {
 };
 
 // Validation and all integer work of a plan; touches no device.
-ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
+ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks, const int64_t *doc_len,
                             const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape, HostPlan *hp) {
     if (!tasks || !doc_len || !doc_kv_offset || !shape) return fail(CA_ERR_INVALID_ARG, "NULL argument");
     if (n_tasks < 1) return fail(CA_ERR_INVALID_ARG, "n_tasks must be >= 1");
@@ -242,7 +245,18 @@ ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64
         d.doc = T.doc_id;
         d.kv_off = static_cast<int32_t>(doc_kv_offset[T.doc_id]);
         d.doc_len = static_cast<int32_t>(L);
-        p->task_pairs[t] = task_pairs_closed_form(T.q_start, T.q_len, T.kv_start, T.kv_len);
+        d.sink = d.lo = d.win = 0;
+        if (masks) {
+            const ca_mask_t &M = masks[t];
+            if (M.sink < 0 || M.lo < 0 || M.window < 0 || M.sink > L || M.lo > L || M.window > L)
+                return fail(CA_ERR_INVALID_ARG, tn + "mask fields must lie in [0, document length]");
+            d.sink = static_cast<int32_t>(M.sink);
+            d.lo = static_cast<int32_t>(M.lo);
+            d.win = static_cast<int32_t>(M.window);
+        }
+        const bool plain = d.sink == 0 && d.lo == 0 && d.win == 0;
+        p->task_pairs[t] = plain ? task_pairs_closed_form(T.q_start, T.q_len, T.kv_start, T.kv_len)
+                                 : task_pairs_rows(d);
         p->pairs += p->task_pairs[t];
         row0 += T.q_len;
     }
@@ -250,14 +264,20 @@ ca_status_t build_host_plan(const ca_task_t *tasks, int32_t n_tasks, const int64
 
     // forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1),
     // longest first; the second tile is absent past the task's last tile.
-    // n_kv = key tiles of the later tile (the earlier tile needs a prefix).
+    // n_kv = key tiles the pair visits (key_tile_ranges over both tiles' rows;
+    // each tile needs a prefix of that sequence).
     std::vector<FwdItem> &fwd = hp->fwd;
     for (int32_t t = 0; t < n_tasks; ++t) {
         const DevTask &d = p->h_tasks[t];
         const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
         for (int32_t tile = 0; tile < ntiles; tile += 2) {
-            const int32_t na = fwd_tile_nkv(d, tile, p->tpt);
-            const int32_t nb = tile + 1 < ntiles ? fwd_tile_nkv(d, tile + 1, p->tpt) : 0;
+            const int32_t p0 = d.q_start + tile * p->tpt;
+            const int32_t end0 = std::min(p0 + p->tpt, d.q_start + d.q_len) - 1;
+            const bool has_b = tile + 1 < ntiles;
+            const int32_t end1 = has_b ? std::min(p0 + 2 * p->tpt, d.q_start + d.q_len) - 1 : end0;
+            const KeyTileRanges r = key_tile_ranges(d, p0, end1);
+            const int32_t na = visits_upto(r, d, end0);
+            const int32_t nb = has_b ? visits_upto(r, d, end1) : 0;
             for (int32_t g = 0; g < p->hkv; ++g) fwd.push_back({t, g, tile, std::max(na, nb)});
             p->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
         }
@@ -336,12 +356,12 @@ void fill_info(const ca_plan *p, ca_plan_info_t *o) {
 
 }  // namespace
 
-ca_status_t ca_plan_dry_run(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
-                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape,
-                            ca_plan_info_t *info, int64_t *task_pairs) {
+ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
+                                   const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
+                                   const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs) {
     if (!info) return fail(CA_ERR_INVALID_ARG, "info is NULL");
     HostPlan hp;
-    ca_status_t st = build_host_plan(tasks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st = build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
     if (st == CA_OK) {
         fill_info(hp.p, info);
         if (task_pairs) std::copy(hp.p->task_pairs.begin(), hp.p->task_pairs.end(), task_pairs);
@@ -350,13 +370,25 @@ ca_status_t ca_plan_dry_run(const ca_task_t *tasks, int32_t n_tasks, const int64
     return st;
 }
 
+ca_status_t ca_plan_dry_run(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
+                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape,
+                            ca_plan_info_t *info, int64_t *task_pairs) {
+    return ca_plan_dry_run_masked(tasks, nullptr, n_tasks, doc_len, doc_kv_offset, n_docs, shape, info, task_pairs);
+}
+
 ca_status_t ca_plan_create(const ca_task_t *tasks, int32_t n_tasks, const int64_t *doc_len,
                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape,
                            void *upload_stream, ca_plan_t **out) {
+    return ca_plan_create_masked(tasks, nullptr, n_tasks, doc_len, doc_kv_offset, n_docs, shape, upload_stream, out);
+}
+
+ca_status_t ca_plan_create_masked(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
+                                  const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
+                                  const ca_shape_t *shape, void *upload_stream, ca_plan_t **out) {
     if (!out) return fail(CA_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     HostPlan hp;
-    ca_status_t st = build_host_plan(tasks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st = build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
     if (st != CA_OK) {
         delete hp.p;
         return st;

@@ -120,6 +120,44 @@ ca_status_t ca_plan_dry_run(const ca_task_t *tasks, int32_t n_tasks,
                             const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
                             const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs);
 
+/*
+ * Sparse visibility of one task ("DCP: Addressing Input Dynamism In
+ * Long-Context Training via Dynamic Context Parallelism", §2.4 and Figure 6:
+ * lambda-shaped sink + sliding window, causal blockwise, shared question
+ * masks).  Row p of the
+ * task sees key j iff the plain rule holds (kv_start <= j < kv_start+kv_len,
+ * j <= p) AND
+ *     j < sink  OR  j >= max(lo, p - window + 1)        (window = 0: j >= lo)
+ * The three families map onto it as:
+ *   lambda:           sink = S, lo = 0, window = W         (one task per shard)
+ *   causal blockwise: per block of B tokens, a task of its rows with
+ *                     sink = (sink blocks) * B, lo = (first visible block) * B,
+ *                     window = 0; the final (test) block a plain task
+ *   shared question:  the question a plain task; answer i a task of its rows
+ *                     with sink = question length, lo = start of answer i
+ * {0, 0, 0} is the plain rule.  All three fields >= 0 and <= the document
+ * length.
+ */
+typedef struct {
+    int64_t sink;
+    int64_t lo;
+    int64_t window;
+} ca_mask_t;
+
+/*
+ * ca_plan_create / ca_plan_dry_run with a mask per task (masks[n_tasks];
+ * NULL = every task plain).  The pair counts, FLOPs and tile lists count only
+ * visible pairs and tiles with at least one visible pair.  Extra errors:
+ * CA_ERR_INVALID_ARG for a negative mask field or one above the document
+ * length.
+ */
+ca_status_t ca_plan_create_masked(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
+                                  const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
+                                  const ca_shape_t *shape, void *upload_stream, ca_plan_t **out);
+ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
+                                   const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
+                                   const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs);
+
 /* Sizes and integer accounting of a plan (all exact, int64). */
 ca_status_t ca_plan_info(const ca_plan_t *plan, ca_plan_info_t *out);
 

@@ -51,6 +51,9 @@ class _Problem(ctypes.Structure):
         ("t_kv_start", ctypes.c_void_p),
         ("t_kv_len", ctypes.c_void_p),
         ("t_row0", ctypes.c_void_p),
+        ("t_sink", ctypes.c_void_p),
+        ("t_lo", ctypes.c_void_p),
+        ("t_win", ctypes.c_void_p),
         ("n_docs", ctypes.c_int32),
         ("doc_len", ctypes.c_void_p),
         ("doc_kv_offset", ctypes.c_void_p),
@@ -76,6 +79,8 @@ def lib():
             L.orc_num_threads.restype = ctypes.c_int
             L.orc_visible_count.restype = i64
             L.orc_visible_count.argtypes = [i64, i64, i64]
+            L.orc_visible_count_masked.restype = i64
+            L.orc_visible_count_masked.argtypes = [i64, i64, i64, i64, i64, i64]
             L.orc_task_pairs.restype = None
             L.orc_task_pairs.argtypes = [i32, vp, vp, vp, vp, vp]
             pb = ctypes.POINTER(_Problem)
@@ -124,6 +129,11 @@ class Problem:
         self.t_kv_start = np.ascontiguousarray(w.task_kv_start, dtype=np.int64)
         self.t_kv_len = np.ascontiguousarray(w.task_kv_len, dtype=np.int64)
         self.t_row0 = np.ascontiguousarray(w.task_row_offset(), dtype=np.int64)
+        sink, lo, win = w.masks()
+        self.t_sink = np.ascontiguousarray(sink, dtype=np.int64)
+        self.t_lo = np.ascontiguousarray(lo, dtype=np.int64)
+        self.t_win = np.ascontiguousarray(win, dtype=np.int64)
+        masked = bool(self.t_sink.any() or self.t_lo.any() or self.t_win.any())
         self.doc_len = np.ascontiguousarray(w.doc_len, dtype=np.int64)
         self.doc_kv_offset = np.ascontiguousarray(w.doc_kv_offset, dtype=np.int64)
         self.total_q = w.total_q
@@ -135,6 +145,8 @@ class Problem:
         self.s = _Problem(
             w.n_tasks, _ptr(self.t_doc).value, _ptr(self.t_q_start).value, _ptr(self.t_q_len).value,
             _ptr(self.t_kv_start).value, _ptr(self.t_kv_len).value, _ptr(self.t_row0).value,
+            (_ptr(self.t_sink).value if masked else None), (_ptr(self.t_lo).value if masked else None),
+            (_ptr(self.t_win).value if masked else None),
             w.n_docs, _ptr(self.doc_len).value, _ptr(self.doc_kv_offset).value,
             hq, hkv, d, float(w.softmax_scale),
             _ptr(self.q).value, _ptr(self.k).value, _ptr(self.v).value,
@@ -146,13 +158,23 @@ class Problem:
 
 
 def task_pairs(w) -> np.ndarray:
-    """Causal (token, key) pairs of every task, per head, int64."""
+    """Visible (token, key) pairs of every task, per head, int64."""
     n = w.n_tasks
     out = np.zeros(n, dtype=np.int64)
     a = [np.ascontiguousarray(x, dtype=np.int64) for x in
          (w.task_q_start, w.task_q_len, w.task_kv_start, w.task_kv_len)]
     lib().orc_task_pairs(n, *[_ptr(x) for x in a], _ptr(out))
+    sink, lo, win = w.masks()
+    for t in range(n):  # masked tasks: the per-key count of the visibility rule
+        if sink[t] or lo[t] or win[t]:
+            qs, ql, ks, kl = (int(x[t]) for x in a)
+            out[t] = sum(lib().orc_visible_count_masked(p, ks, kl, int(sink[t]), int(lo[t]), int(win[t]))
+                         for p in range(qs, qs + ql))
     return out
+
+
+def visible_count_masked(p, kv_start, kv_len, sink, lo, window) -> int:
+    return int(lib().orc_visible_count_masked(p, kv_start, kv_len, sink, lo, window))
 
 
 def flops(w):

@@ -19,6 +19,11 @@
  *   in q(t)").  kv_start/kv_len express one KV block of a split context
  *   (Context Parallelism for Scalable Million-Token Inference, §3.5.2
  *   pass-KV); the prefix task is kv_start = 0, kv_len = q_start + q_len.
+ *   A task may carry a sparse mask (sink, lo, window) ("DCP: Addressing
+ *   Input Dynamism In Long-Context Training via Dynamic Context
+ *   Parallelism", §2.4, Figure 6: attention sink + sliding window, causal
+ *   blockwise, shared question): j in V(p) additionally needs
+ *       j < sink  or  j >= max(lo, p - window + 1)    (window 0: j >= lo).
  *
  *   For query head h the kv head is g = floor(h / G), G = H_q / H_kv
  *   (contiguous GQA grouping).  With s_pj = scale * q_p . k_j:
@@ -62,6 +67,7 @@ typedef struct {
     const int32_t *t_doc;
     const int64_t *t_q_start, *t_q_len, *t_kv_start, *t_kv_len;
     const int64_t *t_row0; /* first packed query row of each task */
+    const int64_t *t_sink, *t_lo, *t_win; /* per-task sparse mask; NULL = none */
     int32_t n_docs;
     const int64_t *doc_len, *doc_kv_offset;
     int32_t hq, hkv, d;
@@ -90,6 +96,28 @@ int64_t orc_visible_count(int64_t p, int64_t kv_start, int64_t kv_len) {
     int64_t hi = kv_start + kv_len - 1; /* last key of the block */
     if (p < hi) hi = p;                 /* causal: j <= p */
     return hi >= kv_start ? hi - kv_start + 1 : 0;
+}
+
+/* The sparse part of the visibility rule for key j of row p. */
+static int mask_allows(int64_t p, int64_t j, int64_t sink, int64_t lo, int64_t window) {
+    if (j < sink) return 1;
+    if (j < lo) return 0;
+    return window == 0 || j >= p - window + 1;
+}
+
+/* |V(p)| of a masked task: every key of the block up to p, tested one by one. */
+int64_t orc_visible_count_masked(int64_t p, int64_t kv_start, int64_t kv_len, int64_t sink, int64_t lo,
+                                 int64_t window) {
+    int64_t n = 0;
+    for (int64_t j = kv_start; j < kv_start + kv_len && j <= p; ++j) n += mask_allows(p, j, sink, lo, window);
+    return n;
+}
+
+/* Whether row p of task t sees key j. */
+static int sees(const orc_problem *pb, int32_t t, int64_t p, int64_t j) {
+    if (j < pb->t_kv_start[t] || j >= pb->t_kv_start[t] + pb->t_kv_len[t] || j > p) return 0;
+    if (!pb->t_sink) return 1;
+    return mask_allows(p, j, pb->t_sink[t], pb->t_lo[t], pb->t_win[t]);
 }
 
 /* Causal pairs of every task: sum over its rows of |V(p)|. */
@@ -130,7 +158,9 @@ static int64_t row_forward(const orc_problem *pb, int64_t r, int32_t h,
     const int64_t base = pb->doc_kv_offset[doc];
     const int32_t G = pb->hq / pb->hkv, g = h / G, d = pb->d;
     const int64_t j0 = pb->t_kv_start[t];
-    const int64_t n = orc_visible_count(p, j0, pb->t_kv_len[t]);
+    const int64_t j1 = j0 + orc_visible_count(p, j0, pb->t_kv_len[t]); /* keys [j0, j1) pass the block and causal tests */
+    int64_t n = 0;
+    for (int64_t j = j0; j < j1; ++j) n += sees(pb, t, p, j);
     const uint16_t *qr = qrow(pb, pb->q, r, h);
     for (int c = 0; c < d; ++c) { qv[c] = bf(qr[c]); o[c] = 0.0; }
     if (n == 0) {
@@ -140,7 +170,8 @@ static int64_t row_forward(const orc_problem *pb, int64_t r, int32_t h,
     }
     /* pass 1: max of the scaled scores */
     double m = -INFINITY;
-    for (int64_t j = j0; j < j0 + n; ++j) {
+    for (int64_t j = j0; j < j1; ++j) {
+        if (!sees(pb, t, p, j)) continue;
         const uint16_t *kr = kvrow(pb, pb->k, base + j, g);
         double s = 0.0;
         for (int c = 0; c < d; ++c) s += qv[c] * bf(kr[c]);
@@ -149,7 +180,8 @@ static int64_t row_forward(const orc_problem *pb, int64_t r, int32_t h,
     }
     /* pass 2: normaliser */
     double sum = 0.0;
-    for (int64_t j = j0; j < j0 + n; ++j) {
+    for (int64_t j = j0; j < j1; ++j) {
+        if (!sees(pb, t, p, j)) continue;
         const uint16_t *kr = kvrow(pb, pb->k, base + j, g);
         double s = 0.0;
         for (int c = 0; c < d; ++c) s += qv[c] * bf(kr[c]);
@@ -157,7 +189,8 @@ static int64_t row_forward(const orc_problem *pb, int64_t r, int32_t h,
     }
     const double L = m + log(sum);
     /* pass 3: O = sum_j P_pj v_j with P_pj = exp(s_pj - LSE) */
-    for (int64_t j = j0; j < j0 + n; ++j) {
+    for (int64_t j = j0; j < j1; ++j) {
+        if (!sees(pb, t, p, j)) continue;
         const uint16_t *kr = kvrow(pb, pb->k, base + j, g);
         const uint16_t *vr = kvrow(pb, pb->v, base + j, g);
         double s = 0.0;
@@ -243,8 +276,9 @@ int orc_dq_rows(const orc_problem *pb, int64_t n_rows, const int64_t *rows,
                 const int32_t g = h / (pb->hq / pb->hkv);
                 const uint16_t *dor = qrow(pb, pb->dout, r, h);
                 for (int c = 0; c < d; ++c) dov[c] = bf(dor[c]);
-                const int64_t j0 = pb->t_kv_start[t];
-                for (int64_t j = j0; j < j0 + n; ++j) {
+                const int64_t p = pb->t_q_start[t] + (r - pb->t_row0[t]);
+                for (int64_t j = pb->t_kv_start[t]; j <= p && j < pb->t_kv_start[t] + pb->t_kv_len[t]; ++j) {
+                    if (!sees(pb, t, p, j)) continue;
                     const uint16_t *kr = kvrow(pb, pb->k, base + j, g);
                     const uint16_t *vr = kvrow(pb, pb->v, base + j, g);
                     double s = 0.0, dP = 0.0;
@@ -282,7 +316,7 @@ static void dkdv_column(const orc_problem *pb, int32_t doc, int64_t j, int32_t g
         if (j < pb->t_kv_start[t] || j >= pb->t_kv_start[t] + pb->t_kv_len[t]) continue;
         for (int64_t i = 0; i < pb->t_q_len[t]; ++i) {
             const int64_t p = pb->t_q_start[t] + i;
-            if (p < j) continue;
+            if (!sees(pb, t, p, j)) continue;
             const int64_t r = pb->t_row0[t] + i;
             for (int32_t h = g * G; h < (g + 1) * G; ++h) {
                 const size_t ix = (size_t)r * pb->hq + h;

@@ -50,7 +50,17 @@ def test_status_strings_and_version():
 WORKLOADS = [W.tiny_chunk(), W.llama8b_chunk(), W.rebatched_pool(), W.long_context_chunk(),
              W.split_kv_prefill(), W.split_kv_prefill(split=False),
              W.custom("kv_blocks", [300], [(0, 200, 100, 0, 64), (0, 200, 100, 64, 200), (0, 5, 20, 100, 7)],
-                      4, 1, 128)]
+                      4, 1, 128),
+             W.lambda_chunk(total=16384), W.blockwise_chunk(total=16384), W.shared_question_pool(total=16384)]
+
+MASKED_SMALL = [
+    W.lambda_chunk(seed=1, total=3000, sink=70, window=300, hq=8, hkv=2, d=64),
+    W.lambda_chunk(seed=2, total=3000, sink=0, window=129, hq=4, hkv=1, d=128),
+    W.blockwise_chunk(seed=3, total=3000, block=96, sink_blocks=2, window_blocks=3, hq=8, hkv=1, d=64),
+    W.shared_question_pool(seed=4, total=3000, q_lo=100, q_hi=400, a_lo=40, a_hi=300, hq=4, hkv=1, d=64),
+    W.custom("mixed_masks", [700, 500], [(0, 0, 700, 0, 700), (1, 100, 300, 50, 400), (0, 300, 200, 0, 600)],
+             8, 2, 64, masks=[(10, 0, 200), (0, 256, 0), (130, 400, 77)]),
+]
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w.name)
@@ -62,6 +72,47 @@ def test_pair_accounting_bit_exact(w):
     fwd, bwd = oracle.flops(w)
     assert info["flops_fwd"] == fwd and info["flops_bwd"] == bwd
     assert info["total_q"] == w.total_q and info["total_kv"] == w.total_kv
+
+
+def visible_block(w, t, p_lo, p_hi, k0, k1):
+    """Whether any row p in [p_lo, p_hi] of task t sees any key in [k0, k1]."""
+    sink, lo, win = (int(x[t]) for x in w.masks())
+    a, e = int(w.task_kv_start[t]), int(w.task_kv_start[t] + w.task_kv_len[t])
+    p = np.arange(p_lo, p_hi + 1)[:, None]
+    j = np.arange(k0, k1 + 1)[None, :]
+    vis = (j >= a) & (j < e) & (j <= p)
+    if sink or lo or win:
+        vis &= (j < sink) | ((j >= lo) & ((win == 0) | (j >= p - win + 1)))
+    return bool(vis.any())
+
+
+def masked_tile_pairs_reference(w):
+    G = w.num_q_heads // w.num_kv_heads
+    T = 128 // G
+    n = 0
+    for t in range(w.n_tasks):
+        q0, ql = int(w.task_q_start[t]), int(w.task_q_len[t])
+        L = int(w.doc_len[w.task_doc[t]])
+        for tile in range((ql + T - 1) // T):
+            p_lo = q0 + tile * T
+            p_hi = min(q0 + ql, p_lo + T) - 1
+            for jt in range((L + 127) // 128):
+                n += visible_block(w, t, p_lo, p_hi, jt * 128, min(L, jt * 128 + 128) - 1)
+    return n * w.num_kv_heads
+
+
+@pytest.mark.parametrize("w", MASKED_SMALL, ids=lambda w: w.name)
+def test_masked_tile_lists(w):
+    """Backward: exactly the (key tile, query tile) pairs with a visible pair.
+    Forward: those, plus at most one extra key tile per query tile where the
+    two tiles of an item start their windows in different key tiles."""
+    info, pairs = ca.dry_run_workload(w)
+    assert np.array_equal(pairs, oracle.task_pairs(w))
+    ref = masked_tile_pairs_reference(w)
+    assert info["bwd_tile_pairs"] == ref
+    G = w.num_q_heads // w.num_kv_heads
+    n_qtiles = sum(-(-int(x) // (128 // G)) for x in w.task_q_len) * w.num_kv_heads
+    assert ref <= info["fwd_tile_pairs"] <= ref + n_qtiles
 
 
 def tile_pairs_reference(w):
@@ -85,7 +136,7 @@ def tile_pairs_reference(w):
     return n * w.num_kv_heads
 
 
-@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[-1], W.rebatched_pool(total_q=4096, doc_lo=1000,
+@pytest.mark.parametrize("w", [WORKLOADS[0], WORKLOADS[6], W.rebatched_pool(total_q=4096, doc_lo=1000,
                                                                               doc_hi=3000, shard_lo=50,
                                                                               shard_hi=700)],
                          ids=lambda w: w.name)

@@ -36,7 +36,11 @@ __all__ = [
     "long_context_chunk",
     "split_kv_prefill",
     "custom",
+    "lambda_chunk",
+    "blockwise_chunk",
+    "shared_question_pool",
     "WORKLOADS",
+    "MASKED_WORKLOADS",
     "make_tensors",
 ]
 
@@ -58,6 +62,21 @@ class Workload:
     head_dim: int
     seed: int = 0
     note: str = ""
+    # sparse mask per task ("DCP: Addressing Input Dynamism In Long-Context
+    # Training via Dynamic Context Parallelism", §2.4, Figure 6), None = plain
+    task_sink: Optional[np.ndarray] = None
+    task_lo: Optional[np.ndarray] = None
+    task_win: Optional[np.ndarray] = None
+
+    def masks(self):
+        """(sink, lo, window) int64 arrays, zeros for plain tasks."""
+        z = np.zeros(self.n_tasks, dtype=np.int64)
+        pick = lambda a: z.copy() if a is None else np.asarray(a, dtype=np.int64)  # noqa: E731
+        return pick(self.task_sink), pick(self.task_lo), pick(self.task_win)
+
+    @property
+    def masked(self) -> bool:
+        return any(a is not None and np.any(a) for a in (self.task_sink, self.task_lo, self.task_win))
 
     @property
     def n_docs(self) -> int:
@@ -244,11 +263,13 @@ def split_kv_prefill(seed: int = 0, n_new: int = 4096, cached: int = 131072, n_b
 
 
 def custom(name: str, doc_len, tasks, hq: int, hkv: int, d: int, seed: int = 0,
-           doc_kv_offset=None) -> Workload:
+           doc_kv_offset=None, masks=None) -> Workload:
     """Explicit documents and tasks.  ``tasks`` is a list of
-    (doc, q_start, q_len, kv_start, kv_len)."""
+    (doc, q_start, q_len, kv_start, kv_len); ``masks`` an optional list of
+    (sink, lo, window) per task."""
     doc_len = np.asarray(doc_len, dtype=np.int64)
     t = np.asarray(tasks, dtype=np.int64).reshape(-1, 5)
+    m = None if masks is None else np.asarray(masks, dtype=np.int64).reshape(-1, 3)
     return Workload(
         name=name,
         doc_len=doc_len,
@@ -260,7 +281,86 @@ def custom(name: str, doc_len, tasks, hq: int, hkv: int, d: int, seed: int = 0,
         task_kv_start=t[:, 3].copy(),
         task_kv_len=t[:, 4].copy(),
         num_q_heads=hq, num_kv_heads=hkv, head_dim=d, seed=seed,
+        task_sink=None if m is None else m[:, 0].copy(),
+        task_lo=None if m is None else m[:, 1].copy(),
+        task_win=None if m is None else m[:, 2].copy(),
     )
+
+
+# ---------------------------------------------------------------- sparse mask families
+
+def lambda_chunk(seed: int = 0, total: int = 65536, sink: int = 64, window: int = 4096,
+                 hq: int = 32, hkv: int = 8, d: int = 128) -> Workload:
+    """The 64K lognormal chunk with a lambda-shaped mask on every document:
+    an attention sink of ``sink`` tokens plus a sliding window of ``window``
+    tokens ("DCP ...", §2.4, Figure 6b; window 4096 as in its Figure 14)."""
+    w = llama8b_chunk(seed=seed, total=total)
+    tasks = [(i, 0, int(L), 0, int(L)) for i, L in enumerate(w.doc_len)]
+    masks = [(min(sink, int(L)), 0, min(window, int(L))) for L in w.doc_len]
+    out = custom(f"lambda_chunk_{total // 1024}k_s{sink}_w{window}", w.doc_len, tasks, hq, hkv, d, seed, masks=masks)
+    return out
+
+
+def blockwise_chunk(seed: int = 0, total: int = 65536, block: int = 256, sink_blocks: int = 1,
+                    window_blocks: int = 2, hq: int = 32, hkv: int = 8, d: int = 128) -> Workload:
+    """The 64K lognormal chunk with a causal blockwise mask on every document
+    ("DCP ...", §2.4, Figure 6c): blocks of ``block`` tokens (in-context
+    examples); a token of a non-final block sees, causally, the first
+    ``sink_blocks`` blocks and the last ``window_blocks`` blocks up to its
+    own; the final block (the test example) sees everything before it.  One
+    task per block."""
+    w = llama8b_chunk(seed=seed, total=total)
+    tasks, masks = [], []
+    for i, L in enumerate(int(x) for x in w.doc_len):
+        nb = -(-L // block)
+        for b in range(nb):
+            q0, q1 = b * block, min((b + 1) * block, L)
+            tasks.append((i, q0, q1 - q0, 0, q1))
+            if b == nb - 1:
+                masks.append((0, 0, 0))
+            else:
+                masks.append((min(sink_blocks * block, L), max(0, b - window_blocks + 1) * block, 0))
+    return custom(f"blockwise_chunk_{total // 1024}k_b{block}", w.doc_len, tasks, hq, hkv, d, seed, masks=masks)
+
+
+def shared_question_pool(seed: int = 0, total: int = 65536, q_lo: int = 512, q_hi: int = 4096,
+                         n_ans_lo: int = 2, n_ans_hi: int = 8, a_lo: int = 256, a_hi: int = 2048,
+                         hq: int = 32, hkv: int = 8, d: int = 128) -> Workload:
+    """Documents made of one question and several answers that share it
+    ("DCP ...", §2.4, Figure 6d): the question is causal; answer i sees the
+    whole question and itself causally, not the other answers.  Lengths
+    uniform in the given ranges (numpy PCG64 from ``seed``), documents
+    appended until ``total`` tokens (the last one truncated)."""
+    rng = np.random.default_rng(seed)
+    doc_len, tasks, masks = [], [], []
+    used = 0
+    while used < total:
+        qn = int(rng.integers(q_lo, q_hi, endpoint=True))
+        na = int(rng.integers(n_ans_lo, n_ans_hi, endpoint=True))
+        ans = [int(x) for x in rng.integers(a_lo, a_hi, na, endpoint=True)]
+        L = qn + sum(ans)
+        if used + L > total:  # the last document: keep what fits, cut the answer that crosses
+            room = total - used
+            qn = min(qn, room)
+            keep, acc = [], qn
+            for a in ans:
+                if acc >= room:
+                    break
+                keep.append(min(a, room - acc))
+                acc += keep[-1]
+            ans = keep
+            L = qn + sum(ans)
+        d_ = len(doc_len)
+        doc_len.append(L)
+        tasks.append((d_, 0, qn, 0, qn))
+        masks.append((0, 0, 0))
+        s = qn
+        for a in ans:
+            tasks.append((d_, s, a, 0, s + a))
+            masks.append((qn, s, 0))
+            s += a
+        used += L
+    return custom(f"shared_question_{total // 1024}k", doc_len, tasks, hq, hkv, d, seed, masks=masks)
 
 
 WORKLOADS = {
@@ -269,6 +369,12 @@ WORKLOADS = {
     "pool": rebatched_pool,
     "long": long_context_chunk,
     "splitkv": split_kv_prefill,
+}
+
+MASKED_WORKLOADS = {
+    "lambda": lambda_chunk,
+    "blockwise": blockwise_chunk,
+    "shared_question": shared_question_pool,
 }
 
 
