@@ -270,6 +270,59 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
+def measure_masks(args, dev, stream, causal_pairs):
+    """The sparse mask families on the same 64K lognormal chunk (lambda: sink
+    64 + window 4096; causal blockwise: 256-token blocks, 1 sink block, 2
+    window blocks; and a 64K pool of shared-question documents): fwd+bwd
+    TFLOP/s over the visible pairs (12 d H_q per pair), and the density
+    relative to the causal chunk."""
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    out = {}
+    for name, gen in W.MASKED_WORKLOADS.items():
+        w = gen(seed=args.seed)
+        q, k, v, do = W.make_tensors(w, device=dev)
+        plan = ca.Plan.from_workload(w, stream=stream)
+        info = plan.info()
+        ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+        o, lse = ca.alloc_forward(plan, device=dev)
+        dq, dk, dv = ca.alloc_backward(plan, device=dev)
+        sh = stream.cuda_stream
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+        def step():
+            plan.forward(q, k, v, o, lse, ws, stream=sh)
+            ev[1].record(stream)
+            plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws, stream=sh)
+
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        fwd, tot = [], []
+        for _ in range(max(3, args.steps // 4)):
+            ev[0].record(stream)
+            step()
+            ev[2].record(stream)
+            stream.synchronize()
+            fwd.append(ev[0].elapsed_time(ev[1]))
+            tot.append(ev[0].elapsed_time(ev[2]))
+        if plan.device_status(stream=sh) != 0:
+            raise RuntimeError(f"device error in the {name} mask measurement")
+        f_ms, t_ms = float(np.median(fwd)), float(np.median(tot))
+        pairs = info["causal_pairs"]
+        out[name] = {"workload": w.name, "visible_pairs_per_head": pairs,
+                     "density_vs_causal_chunk": pairs / causal_pairs if name != "shared_question" else None,
+                     "fwd_bwd_ms": t_ms, "forward_ms": f_ms,
+                     "tflops": (info["flops_fwd"] + info["flops_bwd"]) / (t_ms * 1e-3) / 1e12,
+                     "forward_tflops": info["flops_fwd"] / (f_ms * 1e-3) / 1e12}
+        plan.close()
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+    return out
+
+
 def measure_split_kv(args, dev, stream, pk):
     """Partial prefill with split KV: 4096 new tokens at positions
     131072..135167, the 135168-key context cut into 8 contiguous blocks, one
@@ -409,6 +462,9 @@ def run_gpu(args, rank, world, local):
     split_kv = None
     if not args.no_split_kv:
         split_kv = measure_split_kv(args, dev, stream, pk)
+    masks = None
+    if not args.no_masks:
+        masks = measure_masks(args, dev, stream, info["causal_pairs"])
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
     peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     main_tf = info["flops_bwd"] / (main_ms * 1e-3) / 1e12
@@ -453,6 +509,7 @@ def run_gpu(args, rank, world, local):
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
             "e2e": e2e,
             "split_kv_prefill": split_kv,
+            "sparse_masks": masks,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -473,6 +530,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-split-kv", action="store_true", help="skip the split-KV prefill + merge measurement")
+    ap.add_argument("--no-masks", action="store_true", help="skip the sparse-mask measurement")
     ap.add_argument("--tokens", type=int, default=65536,
                     help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()
