@@ -55,7 +55,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in a thread;
+    the summary keeps the samples read between mark_start() and mark_end()."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -66,12 +67,13 @@ class ClockSampler:
         self.rows = []
         self.proc = None
         self.thread = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -82,7 +84,13 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9:
-                self.rows.append(parts)
+                self.rows.append((time.time(), parts))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is not None:
@@ -100,16 +108,42 @@ class ClockSampler:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        rows = [r for t, r in self.rows
+                if self.t0 is None or self.t1 is None or self.t0 <= t <= self.t1 + 0.05]
+        if not rows:
+            rows = [r for _, r in self.rows]
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
-        for r in self.rows:
+        for r in rows:
             for n, v in zip(names, r[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def measured_traffic(kernel_file="traffic_bwd_main_llama8b_chunk_64k.json"):
+    """DRAM bytes per launch of the backward main kernel from the committed
+    ncu summary, or None when the kernel's sources have changed since the
+    capture (their hash differs) or no summary exists."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", kernel_file)
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != d["sources_sha256"]:
+            return None
+        return int(d["dram_read_bytes"]) + int(d["dram_write_bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def dist_setup(n_gpus):
@@ -432,6 +466,7 @@ def run_gpu(args, rank, world, local):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
+    clocks.mark_start()
     with torch.cuda.stream(stream):
         start.record(stream)
         for s in range(args.steps):
@@ -439,6 +474,7 @@ def run_gpu(args, rank, world, local):
             step()
         end.record(stream)
     stream.synchronize()
+    clocks.mark_end()
     plan.set_timing_events(None)
     torch.cuda.synchronize()
     barrier(world)
@@ -504,7 +540,8 @@ def run_gpu(args, rank, world, local):
             "parts_tflops": {"forward": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12,
                              "backward": info["flops_bwd"] / ((pre_ms + main_ms + fin_ms) * 1e-3) / 1e12},
             "roofline": {"kernel": "ca_bwd_main_kernel", "bound": "tensor", "achieved": main_tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": measured_traffic(),
+                         "traffic_unit": "bytes per launch (ncu dram read + write, profiles/)",
                          "peak_kind": f"bf16 burst, {pk_kind}",
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
             "e2e": e2e,
