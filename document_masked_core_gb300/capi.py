@@ -28,7 +28,8 @@ CA_DTYPE_FP32 = 1
 
 # names declared in include/ca.h and include/ca_sched.h, in order
 EXPORTS = [
-    "ca_plan_create", "ca_plan_dry_run", "ca_plan_create_masked", "ca_plan_dry_run_masked", "ca_plan_info",
+    "ca_plan_create", "ca_plan_dry_run", "ca_plan_create_masked", "ca_plan_dry_run_masked", "ca_plan_set_kv_split",
+    "ca_plan_info",
     "ca_plan_task_pairs", "ca_plan_destroy",
     "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
@@ -112,6 +113,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.ca_plan_dry_run_masked.restype = st
     L.ca_plan_dry_run_masked.argtypes = [ctypes.POINTER(Task), vp, i32, vp, vp, i32, ctypes.POINTER(Shape),
                                          ctypes.POINTER(PlanInfo), vp]
+    L.ca_plan_set_kv_split.restype = st
+    L.ca_plan_set_kv_split.argtypes = [vp, i32]
     L.ca_plan_info.restype = st
     L.ca_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.ca_plan_task_pairs.restype = st
@@ -281,6 +284,12 @@ class Plan:
         out = PlanInfo()
         _check(load().ca_plan_info(self.handle, ctypes.byref(out)))
         return out.as_dict()
+
+    def set_kv_split(self, visits_per_part: int):
+        """ca_plan_set_kv_split: cut forward items longer than this many key
+        tiles into parts merged in the launch (0 = automatic, < 0 = never).
+        The workspace size may change: allocate it after this call."""
+        _check(load().ca_plan_set_kv_split(self.handle, int(visits_per_part)))
 
     def task_pairs(self) -> np.ndarray:
         out = np.zeros(self.n_tasks, dtype=np.int64)

@@ -48,6 +48,7 @@ struct FwdParams {
     void *o;
     float *lse;
     int32_t *sched;  // work-queue counter (zeroed before the launch)
+    SplitScratch split;  // partial rows of split items and their row counters (zeroed before the launch)
     DevCtl ctl;
 };
 
@@ -99,7 +100,8 @@ struct TileGeo {
 // two query tiles; tile x visits the prefix of n_kv(x) entries that reaches
 // its last row's last visible key (the same rule as the host plan).
 struct ItemGeo {
-    int32_t g, kv_off, n_kv;
+    int32_t g, kv_off, n_kv, i0;
+    int32_t part, nparts, split, slot0;
     KeyTileRanges kr;
     DevTask task;
     TileGeo t[2];
@@ -127,8 +129,16 @@ __device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) 
     const int32_t end0 = gi.t[0].p_first + gi.t[0].ntok - 1;
     const int32_t end1 = gi.t[1].ntok > 0 ? gi.t[1].p_first + gi.t[1].ntok - 1 : end0;
     gi.kr = key_tile_ranges(t, gi.t[0].p_first, end1);
-    gi.t[0].n_kv = gi.t[0].ntok > 0 ? visits_upto(gi.kr, t, end0) : 0;
-    gi.t[1].n_kv = gi.t[1].ntok > 0 ? visits_upto(gi.kr, t, end1) : 0;
+    // this item covers visits [i0, i1) of the pair's sequence
+    gi.i0 = it.i0;
+    gi.part = it.part;
+    gi.nparts = it.nparts;
+    gi.split = it.split;
+    gi.slot0 = it.slot0;
+    const int32_t va = gi.t[0].ntok > 0 ? visits_upto(gi.kr, t, end0) : 0;
+    const int32_t vb = gi.t[1].ntok > 0 ? visits_upto(gi.kr, t, end1) : 0;
+    gi.t[0].n_kv = max(0, min(va, it.i1) - it.i0);
+    gi.t[1].n_kv = max(0, min(vb, it.i1) - it.i0);
     gi.n_kv = max(gi.t[0].n_kv, gi.t[1].n_kv);
     return gi;
 }
@@ -158,6 +168,70 @@ __device__ __forceinline__ void store_row_zero(const FwdParams &p, size_t out_id
         for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
     }
     p.lse[out_idx] = -INFINITY;
+}
+
+// Split items: merge of the parts' partial rows (Eq. 4 of the million-token
+// paper's Appendix B) by the part that finished a row last.  Partials are
+// read through L2 (other SMs wrote them).
+template <int D, bool OUT_F32>
+__device__ __noinline__ void merge_split_row(const FwdParams &p, int32_t nparts, int32_t slot0, int32_t rowslot,
+                                             size_t out_idx) {
+    float M = -INFINITY;
+    for (int32_t s = 0; s < nparts; ++s) M = fmaxf(M, __ldcg(p.split.lse + (slot0 + s) * 256 + rowslot));
+    if (M == -INFINITY) {
+        store_row_zero<D, OUT_F32>(p, out_idx);
+        return;
+    }
+    float wsum = 0.f;
+    for (int32_t s = 0; s < nparts; ++s) wsum += expf(__ldcg(p.split.lse + (slot0 + s) * 256 + rowslot) - M);
+    const float inv = 1.f / wsum;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        for (int32_t s = 0; s < nparts; ++s) {
+            const float w = expf(__ldcg(p.split.lse + (slot0 + s) * 256 + rowslot) - M);
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.split.o + (static_cast<size_t>(slot0 + s) * 256 + rowslot) * D + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 v = __ldcg(src + e);
+                acc[4 * e] += w * v.x;
+                acc[4 * e + 1] += w * v.y;
+                acc[4 * e + 2] += w * v.z;
+                acc[4 * e + 3] += w * v.w;
+            }
+        }
+        if (OUT_F32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(acc[4 * e] * inv, acc[4 * e + 1] * inv, acc[4 * e + 2] * inv, acc[4 * e + 3] * inv);
+        } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pack_bf16(acc[8 * e] * inv, acc[8 * e + 1] * inv),
+                                    pack_bf16(acc[8 * e + 2] * inv, acc[8 * e + 3] * inv),
+                                    pack_bf16(acc[8 * e + 4] * inv, acc[8 * e + 5] * inv),
+                                    pack_bf16(acc[8 * e + 6] * inv, acc[8 * e + 7] * inv));
+        }
+    }
+    p.lse[out_idx] = M + logf(wsum);
+}
+
+// A part's row is in the workspace: count it, and merge the row if this part
+// was the last of the item's parts to get there.
+template <int D, bool OUT_F32>
+__device__ __forceinline__ void finish_split_row(const FwdParams &p, const ItemGeo &gi, int32_t rowslot,
+                                                 size_t out_idx) {
+    __threadfence();
+    const int32_t done = atomicAdd(p.split.cnt + gi.split * 256 + rowslot, 1);
+    if (done == gi.nparts - 1) {
+        __threadfence();
+        merge_split_row<D, OUT_F32>(p, gi.nparts, gi.slot0, rowslot, out_idx);
+    }
 }
 
 template <int D, bool OUT_F32>
@@ -245,7 +319,7 @@ __global__ void __launch_bounds__(320, 1)
                     const uint32_t st = kv_it % C::kStages;
                     const uint32_t ph = (kv_it / C::kStages) & 1;
                     if (!(ok = mbar_wait(&bars.kv_empty[st], ph ^ 1, wd))) break;
-                    const int32_t key_row = gi.kv_off + gi.kr.tile(i) * kTileKeys;
+                    const int32_t key_row = gi.kv_off + gi.kr.tile(gi.i0 + i) * kTileKeys;
                     mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
@@ -360,8 +434,21 @@ __global__ void __launch_bounds__(320, 1)
             const int32_t pos = tg.p_first + min(tok, max(tg.ntok - 1, 0));
             const RowKeys rk = row_keys(gi.task, pos);  // visible keys: [a, r1) U [r2, hi)
             const size_t out_idx = static_cast<size_t>(tg.row0 + tok) * p.hq + h;
+            const bool split = gi.nparts > 1;
+            const int32_t rowslot = x * 128 + static_cast<int32_t>(row);
+            float *part_o = p.split.o + (static_cast<size_t>(gi.slot0 + gi.part) * 256 + rowslot) * D;
             if (tg.n_kv == 0) {
-                if (valid) store_row_zero<D, OUT_F32>(p, out_idx);
+                if (valid) {
+                    if (split) {  // this part sees none of the tile's keys: an empty partial
+                        float4 *dst = reinterpret_cast<float4 *>(part_o);
+#pragma unroll
+                        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        p.split.lse[(gi.slot0 + gi.part) * 256 + rowslot] = -INFINITY;
+                        finish_split_row<D, OUT_F32>(p, gi, rowslot, out_idx);
+                    } else {
+                        store_row_zero<D, OUT_F32>(p, out_idx);
+                    }
+                }
                 continue;
             }
             float m = -INFINITY, l = 0.f;
@@ -376,7 +463,7 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-                const int32_t key0 = gi.kr.tile(i) * kTileKeys;
+                const int32_t key0 = gi.kr.tile(gi.i0 + i) * kTileKeys;
                 const bool whole = (key0 >= rk.a && key0 + kTileKeys <= rk.r1) ||
                                    (key0 >= rk.a && key0 >= rk.r2 && key0 + kTileKeys <= rk.hi);
                 if (!whole) {
@@ -452,7 +539,14 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_ld32(o_addr + c * 32, orr);
                 tmem_ld_wait();
                 reg_fence(orr);
-                if (valid) {
+                if (valid && split) {
+                    float4 *dst = reinterpret_cast<float4 *>(part_o + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(orr[4 * e]) * inv_l, __uint_as_float(orr[4 * e + 1]) * inv_l,
+                                             __uint_as_float(orr[4 * e + 2]) * inv_l,
+                                             __uint_as_float(orr[4 * e + 3]) * inv_l);
+                } else if (valid) {
                     if (OUT_F32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D + c * 32);
 #pragma unroll
@@ -482,7 +576,13 @@ __global__ void __launch_bounds__(320, 1)
             }
             tc_fence_before();
             mbar_arrive(&bars.o_empty[x]);
-            if (valid) p.lse[out_idx] = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+            const float lse_row = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+            if (valid && split) {
+                p.split.lse[(gi.slot0 + gi.part) * 256 + rowslot] = lse_row;
+                finish_split_row<D, OUT_F32>(p, gi, rowslot, out_idx);
+            } else if (valid) {
+                p.lse[out_idx] = lse_row;
+            }
         }
     }
 
@@ -517,6 +617,11 @@ cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, cons
     int32_t *sched = work_counters(pl, workspace) + 1;
     cudaError_t e0 = cudaMemsetAsync(sched, 0, sizeof(int32_t), stream);
     if (e0 != cudaSuccess) return e0;
+    const SplitScratch split = split_scratch(pl, workspace);
+    if (pl->n_split > 0) {  // row counters of the split items start at zero
+        e0 = cudaMemsetAsync(split.cnt, 0, static_cast<size_t>(pl->n_split) * 256 * sizeof(int32_t), stream);
+        if (e0 != cudaSuccess) return e0;
+    }
     CUtensorMap tq, tk, tv;
     if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
         make_tmap_3d(&tk, k, pl->total_kv, pl->hkv, pl->d, 1, kTileKeys) != CA_OK ||
@@ -533,6 +638,7 @@ cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, cons
     prm.o = o;
     prm.lse = lse;
     prm.sched = sched;
+    prm.split = split;
     prm.ctl.err = pl->d_err;
     prm.ctl.wait_limit_ns = static_cast<unsigned long long>(pl->wait_limit_ns);
     const bool f32 = pl->o_dtype == CA_DTYPE_FP32;

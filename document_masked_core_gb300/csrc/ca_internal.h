@@ -123,9 +123,14 @@ __host__ __device__ inline void key_tile_rows(const DevTask &t, int32_t k0, int3
 
 // Forward item: query tiles `tile` and `tile + 1` (tile even; tokens
 // [tile*T, tile*T+2T) of the task, T = 128 / G) of kv head g, processed
-// together by one CTA; n_kv = visible 128-key tiles of the later tile.
+// together by one CTA, over visits [i0, i1) of the pair's key-tile sequence
+// (n_kv = i1 - i0).  A pair split into nparts > 1 items writes partial
+// (O, LSE) rows to slots slot0 + part of the workspace; the last part to
+// finish a row merges the parts (per-row counters of split pair `split`).
 struct FwdItem {
     int32_t task, g, tile, n_kv;
+    int32_t i0, i1, part, nparts;
+    int32_t split, slot0;
 };
 
 // Backward tile: key tile kv_tile of document doc, kv head g; n_q = number of
@@ -157,6 +162,9 @@ struct ca_plan {
     std::vector<ca::DevTask> h_tasks;
     int64_t n_fwd = 0, n_bwd = 0;
     int64_t workspace_bytes = 0;
+    int32_t kv_split = 0;                 // 0: automatic, < 0: never split, > 0: visits per part
+    int64_t n_split = 0, n_slots = 0;     // split pairs, partial slots (256 rows each)
+    int64_t split_ws_off = 0;             // workspace offset of the partial O / LSE / counters
     int64_t wait_limit_ns = 2000000000LL;
     void *const *timing_events = nullptr;  // optional cudaEvent_t[6], see ca_plan_set_timing_events
     int device = 0, num_sms = 0;
@@ -188,12 +196,27 @@ inline cudaError_t mark(const ca_plan *p, int slot, cudaStream_t stream) {
     return cudaEventRecord(static_cast<cudaEvent_t>(p->timing_events[slot]), stream);
 }
 
-// Work-queue counters at the end of the workspace (256 bytes after the fp32
-// dQ accumulator and the D vector): [0] backward main kernel, [1] forward.
+// Work-queue counters (256 bytes after the fp32 dQ accumulator and the D
+// vector): [0] backward main kernel, [1] forward.
 inline int32_t *work_counters(const ca_plan *p, void *workspace) {
     const int64_t units = p->total_q * p->hq;
     const int64_t off = (units * p->d * 4 + 255) / 256 * 256 + (units * 4 + 255) / 256 * 256;
     return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + off);
+}
+
+// Split-KV forward scratch after the counters: partial O [n_slots][256][d]
+// fp32, partial LSE [n_slots][256] fp32, row counters [n_split][256] int32.
+struct SplitScratch {
+    float *o, *lse;
+    int32_t *cnt;
+};
+inline SplitScratch split_scratch(const ca_plan *p, void *workspace) {
+    uint8_t *base = static_cast<uint8_t *>(workspace) + p->split_ws_off;
+    SplitScratch s;
+    s.o = reinterpret_cast<float *>(base);
+    s.lse = reinterpret_cast<float *>(base + p->n_slots * 256 * p->d * 4);
+    s.cnt = reinterpret_cast<int32_t *>(base + p->n_slots * 256 * (p->d + 1) * 4);
+    return s;
 }
 
 cudaError_t launch_forward(const ca_plan *p, const void *q, const void *k, const void *v, void *o,

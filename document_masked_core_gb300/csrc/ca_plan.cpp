@@ -168,6 +168,79 @@ const char *ca_last_error(void) { return g_last_error.c_str(); }
 
 namespace {
 
+// Workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned, 256 bytes
+// of work-queue counters, then the split-KV forward scratch (split_scratch).
+void set_workspace_bytes(ca_plan *p) {
+    const int64_t rows_heads = p->total_q * p->hq;
+    const int64_t dq_bytes = (rows_heads * p->d * 4 + 255) / 256 * 256;
+    const int64_t d_bytes = (rows_heads * 4 + 255) / 256 * 256;
+    p->split_ws_off = dq_bytes + d_bytes + 256;
+    const int64_t split_bytes = (p->n_slots * 256 * (p->d + 1) * 4 + p->n_split * 256 * 4 + 255) / 256 * 256;
+    p->workspace_bytes = p->split_ws_off + split_bytes;
+}
+
+// Forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1),
+// longest first; the second tile is absent past the task's last tile.  The
+// pair visits the key tiles of key_tile_ranges over both tiles' rows (each
+// tile a prefix of that sequence).  A pair with more visits than the split
+// size is cut into nparts balanced items over [i0, i1) of its sequence.
+// Split size: kv_split > 0 as given; kv_split < 0 never; kv_split = 0
+// (automatic) only when the launch has fewer than 4 waves of items on a
+// 152-SM GPU, then total visits / 608, at least 8.
+void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
+    std::vector<FwdItem> &fwd = *out;
+    fwd.clear();
+    struct Pair {
+        int32_t t, tile, na, nb, n;
+    };
+    std::vector<Pair> pairs;
+    int64_t total_visits = 0;
+    p->fwd_tile_pairs = 0;
+    for (int32_t t = 0; t < p->n_tasks; ++t) {
+        const DevTask &d = p->h_tasks[t];
+        const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
+        for (int32_t tile = 0; tile < ntiles; tile += 2) {
+            const int32_t p0 = d.q_start + tile * p->tpt;
+            const int32_t end0 = std::min(p0 + p->tpt, d.q_start + d.q_len) - 1;
+            const bool has_b = tile + 1 < ntiles;
+            const int32_t end1 = has_b ? std::min(p0 + 2 * p->tpt, d.q_start + d.q_len) - 1 : end0;
+            const KeyTileRanges r = key_tile_ranges(d, p0, end1);
+            const int32_t na = visits_upto(r, d, end0);
+            const int32_t nb = has_b ? visits_upto(r, d, end1) : 0;
+            pairs.push_back({t, tile, na, nb, std::max(na, nb)});
+            total_visits += static_cast<int64_t>(std::max(na, nb)) * p->hkv;
+            p->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
+        }
+    }
+    constexpr int64_t kWaveUnits = 4 * 152;
+    int64_t chunk = 0;  // 0 = no split
+    if (p->kv_split > 0) {
+        chunk = p->kv_split;
+    } else if (p->kv_split == 0 && static_cast<int64_t>(pairs.size()) * p->hkv < kWaveUnits) {
+        chunk = std::max<int64_t>(8, (total_visits + kWaveUnits - 1) / kWaveUnits);
+    }
+    p->n_split = 0;
+    p->n_slots = 0;
+    for (const Pair &pr : pairs) {
+        const int32_t nparts = (chunk > 0 && pr.n > chunk) ? static_cast<int32_t>((pr.n + chunk - 1) / chunk) : 1;
+        for (int32_t g = 0; g < p->hkv; ++g) {
+            int32_t split = -1, slot0 = 0;
+            if (nparts > 1) {
+                split = static_cast<int32_t>(p->n_split++);
+                slot0 = static_cast<int32_t>(p->n_slots);
+                p->n_slots += nparts;
+            }
+            for (int32_t part = 0; part < nparts; ++part) {
+                const int32_t i0 = static_cast<int32_t>(static_cast<int64_t>(pr.n) * part / nparts);
+                const int32_t i1 = static_cast<int32_t>(static_cast<int64_t>(pr.n) * (part + 1) / nparts);
+                fwd.push_back({pr.t, g, pr.tile, i1 - i0, i0, i1, part, nparts, split, slot0});
+            }
+        }
+    }
+    std::stable_sort(fwd.begin(), fwd.end(), [](const FwdItem &a, const FwdItem &b) { return a.n_kv > b.n_kv; });
+    p->n_fwd = static_cast<int64_t>(fwd.size());
+}
+
 struct HostPlan {
     ca_plan *p = nullptr;
     std::vector<FwdItem> fwd;
@@ -262,28 +335,7 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     }
     p->total_q = row0;
 
-    // forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1),
-    // longest first; the second tile is absent past the task's last tile.
-    // n_kv = key tiles the pair visits (key_tile_ranges over both tiles' rows;
-    // each tile needs a prefix of that sequence).
-    std::vector<FwdItem> &fwd = hp->fwd;
-    for (int32_t t = 0; t < n_tasks; ++t) {
-        const DevTask &d = p->h_tasks[t];
-        const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
-        for (int32_t tile = 0; tile < ntiles; tile += 2) {
-            const int32_t p0 = d.q_start + tile * p->tpt;
-            const int32_t end0 = std::min(p0 + p->tpt, d.q_start + d.q_len) - 1;
-            const bool has_b = tile + 1 < ntiles;
-            const int32_t end1 = has_b ? std::min(p0 + 2 * p->tpt, d.q_start + d.q_len) - 1 : end0;
-            const KeyTileRanges r = key_tile_ranges(d, p0, end1);
-            const int32_t na = visits_upto(r, d, end0);
-            const int32_t nb = has_b ? visits_upto(r, d, end1) : 0;
-            for (int32_t g = 0; g < p->hkv; ++g) fwd.push_back({t, g, tile, std::max(na, nb)});
-            p->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
-        }
-    }
-    std::stable_sort(fwd.begin(), fwd.end(), [](const FwdItem &a, const FwdItem &b) { return a.n_kv > b.n_kv; });
-    p->n_fwd = static_cast<int64_t>(fwd.size());
+    build_fwd_items(p, &hp->fwd);
 
     // documents -> tasks (CSR), and backward tiles: (document, kv head, key tile)
     std::vector<int32_t> &ptr = hp->ptr, &dtasks = hp->dtasks, &doc_info = hp->doc_info;
@@ -330,14 +382,36 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     }
     p->n_bwd = static_cast<int64_t>(bwd.size());
 
-    // workspace: fp32 dQ accumulator + fp32 D, each 256-byte aligned, then 256
-    // bytes of work-queue counters
-    const int64_t rows_heads = p->total_q * p->hq;
-    const int64_t dq_bytes = (rows_heads * p->d * 4 + 255) / 256 * 256;
-    const int64_t d_bytes = (rows_heads * 4 + 255) / 256 * 256;
-    p->workspace_bytes = dq_bytes + d_bytes + 256;
+    set_workspace_bytes(p);
     return CA_OK;
 }
+
+}  // namespace
+
+// Re-cut the forward items with a new split size (see build_fwd_items) and
+// upload them; the workspace size may change.
+extern "C" ca_status_t ca_plan_set_kv_split(ca_plan_t *p, int32_t visits_per_part) {
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    std::vector<FwdItem> fwd;
+    const int32_t old = p->kv_split;
+    p->kv_split = visits_per_part;
+    build_fwd_items(p, &fwd);
+    set_workspace_bytes(p);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) {
+        cudaFree(p->d_fwd);
+        p->d_fwd = nullptr;
+        e = upload(&p->d_fwd, fwd, nullptr);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    }
+    if (e != cudaSuccess) {
+        p->kv_split = old;
+        return cuda_fail(e, "forward item upload");
+    }
+    return CA_OK;
+}
+
+namespace {
 
 void fill_info(const ca_plan *p, ca_plan_info_t *o) {
     o->total_q = p->total_q;

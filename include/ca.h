@@ -158,6 +158,23 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
                                    const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
                                    const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs);
 
+/*
+ * Split-KV inside the forward launch (the pass-KV merge of "Context
+ * Parallelism for Scalable Million-Token Inference", §3.5.2 and Appendix B,
+ * Eq. 4, done in the same launch): a forward item (two query tiles of one
+ * task and kv head) whose key-tile sequence is longer than visits_per_part
+ * tiles is cut into ceil(n / visits_per_part) balanced parts that run on
+ * different SMs; each part writes its rows' partial (O, LSE) to the
+ * workspace and the last part to finish a row merges the parts.  This serves
+ * decode and pass-Q shapes (few query rows, long contexts) and the tail of
+ * very long rows.  visits_per_part > 0: that size; < 0: never split; 0
+ * (the default of every plan): split only when the launch has fewer than 4
+ * waves of items (608 on a 152-SM GPU), to about 608 items.  Rebuilds and
+ * uploads the plan's forward list (synchronises the device first); the
+ * workspace size in ca_plan_info may change.
+ */
+ca_status_t ca_plan_set_kv_split(ca_plan_t *plan, int32_t visits_per_part);
+
 /* Sizes and integer accounting of a plan (all exact, int64). */
 ca_status_t ca_plan_info(const ca_plan_t *plan, ca_plan_info_t *out);
 

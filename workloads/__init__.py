@@ -39,6 +39,7 @@ __all__ = [
     "lambda_chunk",
     "blockwise_chunk",
     "shared_question_pool",
+    "decode_batch",
     "WORKLOADS",
     "MASKED_WORKLOADS",
     "make_tensors",
@@ -361,6 +362,20 @@ def shared_question_pool(seed: int = 0, total: int = 65536, q_lo: int = 512, q_h
             s += a
         used += L
     return custom(f"shared_question_{total // 1024}k", doc_len, tasks, hq, hkv, d, seed, masks=masks)
+
+
+def decode_batch(seed: int = 0, n_seq: int = 16, context: int = 131072, q_len: int = 1, jitter: int = 0,
+                 hq: int = 32, hkv: int = 8, d: int = 128) -> Workload:
+    """Decode / pass-Q shape (Context Parallelism for Scalable Million-Token
+    Inference, §3.5.3-3.5.4: T new tokens per sequence, T = 1 for decode,
+    against a long cached context P): ``n_seq`` documents of ``context``
+    cached tokens (minus a uniform jitter in [0, jitter]) followed by
+    ``q_len`` new tokens, one task per sequence with the prefix context."""
+    rng = np.random.default_rng(seed)
+    ctx = [context - int(rng.integers(0, jitter, endpoint=True)) if jitter else context for _ in range(n_seq)]
+    doc_len = [c + q_len for c in ctx]
+    tasks = [(i, c, q_len, 0, c + q_len) for i, c in enumerate(ctx)]
+    return custom(f"decode_{n_seq}x{context}_t{q_len}_h{hq}x{hkv}_d{d}", doc_len, tasks, hq, hkv, d, seed)
 
 
 WORKLOADS = {
