@@ -357,6 +357,49 @@ def measure_masks(args, dev, stream, causal_pairs):
     return out
 
 
+def measure_decode(args, dev, stream, pk):
+    """Decode shape (one new token per sequence against 131072 cached tokens,
+    16 sequences, 32 q / 8 kv heads): forward time with the in-launch
+    split-KV (automatic) and without it, against the HBM roofline
+    (algorithmic bytes: every K and V row of every sequence read once, Q, O
+    and LSE once)."""
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    w = W.decode_batch(seed=args.seed, n_seq=16, context=131072, q_len=1)
+    q, k, v, _ = W.make_tensors(w, device=dev, need_grad_inputs=False)
+    hbm = float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    nbytes = int(w.doc_len.sum()) * w.num_kv_heads * w.head_dim * 2 * 2 + w.total_q * w.num_q_heads * (
+        w.head_dim * 2 * 2 + 4)
+    out = {"workload": w.name, "algorithmic_bytes": nbytes}
+    for mode, split in (("split", 0), ("unsplit", -1)):
+        plan = ca.Plan.from_workload(w, stream=stream)
+        plan.set_kv_split(split)
+        info = plan.info()
+        ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+        o, lse = ca.alloc_forward(plan, device=dev)
+        sh = stream.cuda_stream
+        for _ in range(args.warmup):
+            plan.forward(q, k, v, o, lse, ws, stream=sh)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(5, args.steps // 4)
+        e0.record(stream)
+        for _ in range(n):
+            plan.forward(q, k, v, o, lse, ws, stream=sh)
+        e1.record(stream)
+        stream.synchronize()
+        if plan.device_status(stream=sh) != 0:
+            raise RuntimeError("device error in the decode measurement")
+        ms = e0.elapsed_time(e1) / n
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[mode] = {"forward_ms": ms, "items": info["n_fwd_items"],
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}}
+        plan.close()
+    return out
+
+
 def measure_split_kv(args, dev, stream, pk):
     """Partial prefill with split KV: 4096 new tokens at positions
     131072..135167, the 135168-key context cut into 8 contiguous blocks, one
@@ -501,6 +544,9 @@ def run_gpu(args, rank, world, local):
     masks = None
     if not args.no_masks:
         masks = measure_masks(args, dev, stream, info["causal_pairs"])
+    decode = None
+    if not args.no_decode:
+        decode = measure_decode(args, dev, stream, pk)
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
     peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     main_tf = info["flops_bwd"] / (main_ms * 1e-3) / 1e12
@@ -547,6 +593,7 @@ def run_gpu(args, rank, world, local):
             "e2e": e2e,
             "split_kv_prefill": split_kv,
             "sparse_masks": masks,
+            "decode": decode,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -568,6 +615,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-split-kv", action="store_true", help="skip the split-KV prefill + merge measurement")
     ap.add_argument("--no-masks", action="store_true", help="skip the sparse-mask measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode (split-KV) measurement")
     ap.add_argument("--tokens", type=int, default=65536,
                     help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()

@@ -186,7 +186,8 @@ void set_workspace_bytes(ca_plan *p) {
 // size is cut into nparts balanced items over [i0, i1) of its sequence.
 // Split size: kv_split > 0 as given; kv_split < 0 never; kv_split = 0
 // (automatic) only when the launch has fewer than 4 waves of items on a
-// 152-SM GPU, then total visits / 608, at least 8.
+// 152-SM GPU: then total visits / 152 clamped to [64, 128] key tiles per
+// part (measured on decode batches of 1 to 32 sequences of 128K tokens).
 void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
     std::vector<FwdItem> &fwd = *out;
     fwd.clear();
@@ -217,7 +218,7 @@ void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
     if (p->kv_split > 0) {
         chunk = p->kv_split;
     } else if (p->kv_split == 0 && static_cast<int64_t>(pairs.size()) * p->hkv < kWaveUnits) {
-        chunk = std::max<int64_t>(8, (total_visits + kWaveUnits - 1) / kWaveUnits);
+        chunk = std::min<int64_t>(128, std::max<int64_t>(64, (total_visits + 151) / 152));
     }
     p->n_split = 0;
     p->n_slots = 0;

@@ -169,7 +169,8 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
  * decode and pass-Q shapes (few query rows, long contexts) and the tail of
  * very long rows.  visits_per_part > 0: that size; < 0: never split; 0
  * (the default of every plan): split only when the launch has fewer than 4
- * waves of items (608 on a 152-SM GPU), to about 608 items.  Rebuilds and
+ * waves of items (608 on a 152-SM GPU), into parts of (total key-tile
+ * visits / 152) clamped to [64, 128] tiles.  Rebuilds and
  * uploads the plan's forward list (synchronises the device first); the
  * workspace size in ca_plan_info may change.
  */

@@ -43,8 +43,9 @@ def forward(w, inputs, split, o_dtype=ca.CA_DTYPE_FP32, backward=False):
 
 SMALL = [W.tiny_chunk()] + EDGE + [
     W.lambda_chunk(seed=1, total=3000, sink=70, window=300, hq=8, hkv=2, d=64),
-    W.decode_batch(seed=2, n_seq=6, context=3000, q_len=1, jitter=700, hq=8, hkv=2, d=128),
-    W.decode_batch(seed=3, n_seq=5, context=2500, q_len=5, jitter=300, hq=16, hkv=1, d=64),
+    # long enough contexts (> 2 x 64 key tiles) for the automatic rule to split
+    W.decode_batch(seed=2, n_seq=6, context=20000, q_len=1, jitter=3000, hq=8, hkv=2, d=128),
+    W.decode_batch(seed=3, n_seq=5, context=17000, q_len=5, jitter=300, hq=16, hkv=1, d=64),
 ]
 
 
