@@ -394,17 +394,21 @@ __global__ void __launch_bounds__(512, 1)
                 bool ok = true;
                 const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), q_base = smem_u32(sQ),
                                do_base = smem_u32(sDO), smem_base = smem_u32(smem);
+                // K and V tiles stay at fixed addresses: their descriptors (K-major for
+                // S^T and dP^T, MN-major for dQ) are built once
+                const uint32_t kd_k = sdesc_lo(k_base, 16), vd_k = sdesc_lo(v_base, 16),
+                               kd_mn = sdesc_lo(k_base, C::kHalfBytes);
                 // S^T = K Q^T of the query tile in ring slot qi
                 auto issue_st = [&](uint32_t qi) -> bool {
                     const uint32_t st = qi % C::kQStages;
                     if (!mbar_wait(&bars.q_full[st], (qi / C::kQStages) & 1, wd)) return false;
                     tc_fence_after();
-                    const uint32_t qb = q_base + st * C::kTileBytes;
+                    const uint32_t qd = sdesc_lo(q_base + st * C::kTileBytes, 16);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                        umma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024),
-                                sdesc_sw128(qb + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                        umma_ss(tmem + C::kColS, sdesc_at(kd_k, off), sdesc_at(qd, off), C::kIdescST,
+                                kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&bars.s_full);
                     return true;
@@ -421,7 +425,9 @@ __global__ void __launch_bounds__(512, 1)
                     if (!(ok = issue_st(qt))) break;
                     for (int32_t j = 0; j < kg.n_q && ok; ++j, ++qt) {
                         const uint32_t st = qt % C::kQStages;
-                        const uint32_t qb = q_base + st * C::kTileBytes, dob = do_base + st * C::kTileBytes;
+                        const uint32_t qd_mn = sdesc_lo(q_base + st * C::kTileBytes, C::kHalfBytes);
+                        const uint32_t dod = sdesc_lo(do_base + st * C::kTileBytes, 16);
+                        const uint32_t dod_mn = sdesc_lo(do_base + st * C::kTileBytes, C::kHalfBytes);
                         // dP^T = V dO^T, once dQ of the previous tile has left the dP^T columns
                         if (!(ok = mbar_wait(&bars.do_full[st], (qt / C::kQStages) & 1, wd))) break;
                         if (!(ok = mbar_wait(&bars.dq_empty, (qt & 1) ^ 1, wd))) break;
@@ -429,8 +435,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                            umma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024),
-                                    sdesc_sw128(dob + off, 16, 1024), C::kIdescST, kk > 0 ? 1u : 0u);
+                            umma_ss(tmem + C::kColDP, sdesc_at(vd_k, off), sdesc_at(dod, off), C::kIdescST,
+                                    kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&bars.dp_full);
                         // dV += P^T dO
@@ -439,9 +445,8 @@ __global__ void __launch_bounds__(512, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDV, tmem + C::kColS + C::packed_col(kk),
-                                    sdesc_sw128(dob + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                    (j == 0 && kk == 0) ? 0u : 1u);
+                            umma_ts(tmem + C::kColDV, tmem + C::kColS + C::packed_col(kk), sdesc_at(dod_mn, kk * 2048),
+                                    C::kIdescAcc, (j == 0 && kk == 0) ? 0u : 1u);
                         if (C::kDsInDo) umma_commit(&bars.dv_done);
                         // S^T of the next query tile of this key tile: the P^T columns
                         // are free once dV (issued above) has read them
@@ -452,17 +457,15 @@ __global__ void __launch_bounds__(512, 1)
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + C::packed_col(kk),
-                                    sdesc_sw128(qb + kk * 2048, C::kHalfBytes, 1024), C::kIdescAcc,
-                                    (j == 0 && kk == 0) ? 0u : 1u);
+                            umma_ts(tmem + C::kColDK, tmem + C::kColDP + C::packed_col(kk), sdesc_at(qd_mn, kk * 2048),
+                                    C::kIdescAcc, (j == 0 && kk == 0) ? 0u : 1u);
                         umma_commit(&bars.q_empty[st]);
                         if (j + 1 == kg.n_q) umma_commit(&bars.acc_full);
-                        const uint32_t dsb = smem_base + C::ds_off(st);
+                        const uint32_t dsd = sdesc_lo(smem_base + C::ds_off(st), C::kHalfBytes);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ss(tmem + C::kColDP, sdesc_sw128(dsb + kk * 2048, C::kHalfBytes, 1024),
-                                    sdesc_sw128(k_base + kk * 2048, C::kHalfBytes, 1024), C::kIdescDQ,
-                                    kk > 0 ? 1u : 0u);
+                            umma_ss(tmem + C::kColDP, sdesc_at(dsd, kk * 2048), sdesc_at(kd_mn, kk * 2048),
+                                    C::kIdescDQ, kk > 0 ? 1u : 0u);
                         umma_commit(&bars.dq_full);
                     }
                     if (!ok) break;

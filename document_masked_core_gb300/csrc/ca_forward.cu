@@ -346,12 +346,13 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t st = kvi % C::kStages;
                 if (!mbar_wait(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
                 tc_fence_after();
+const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
+                const uint32_t bd = sdesc_lo(k_base + st * C::kTileBytes, 16);
+                const uint32_t d_s = tmem + C::kColS + x * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                    const uint64_t ad = sdesc_sw128(q_base + x * C::kTileBytes + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(k_base + st * C::kTileBytes + off, 16, 1024);
-                    umma_ss(tmem + C::kColS + x * 128, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss(d_s, sdesc_at(ad, off), sdesc_at(bd, off), C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars.s_full[x]);
                 return true;
@@ -381,13 +382,12 @@ __global__ void __launch_bounds__(320, 1)
                         if (!(ok = mbar_wait(&bars.p_full[x], s_it[x] & 1, wd))) break;
                         if (i == 0 && !(ok = mbar_wait(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
                         tc_fence_after();
+const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
+                        const uint32_t d_o = tmem + C::kColO + x * D, a_p = tmem + C::kColS + x * 128;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bd =
-                                sdesc_sw128(v_base + st * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
-                            umma_ts(tmem + C::kColO + x * D, tmem + C::kColS + x * 128 + kk * 8, bd, C::kIdescPV,
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_ts(d_o, a_p + kk * 8, sdesc_at(bd, kk * 2048), C::kIdescPV,
                                     (i > 0 || kk > 0) ? 1u : 0u);
-                        }
                         ++s_it[x];
                         if (i + 1 < nk[x]) {
                             if (!(ok = issue_s(x, kvi + 1))) break;

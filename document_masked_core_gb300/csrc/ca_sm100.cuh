@@ -161,16 +161,22 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading
-// and stride byte offsets (16-byte units), version 1, swizzle mode 2 = 128B.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
+// Shared-memory matrix descriptor (tcgen05 format), 128B swizzle: bits 0-13
+// start address >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
+// offset >> 4 (1024 B: eight 128-byte rows), bit 46 version 1, bits 61-63
+// swizzle mode 2.  Only the low word (start address and leading offset)
+// differs between the operands of these kernels, so issuing threads keep low
+// words live and attach the constant high word per instruction, advancing the
+// address by compile-time offsets (multiples of 16 bytes; shared-memory
+// addresses stay below 256 KB, so the 14-bit field never carries).  Rebuilding
+// a whole descriptor per K step was measured to cost about a third of the
+// tensor pipe's rate.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_at(uint32_t lo, uint32_t bytes) {
+    constexpr uint32_t kHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+    return (static_cast<uint64_t>(kHi) << 32) | (lo + (bytes >> 4));
 }
 
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
@@ -258,6 +264,13 @@ __device__ __forceinline__ void regs_increase() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_decrease() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Moves the warpgroup from the launch allocation kLaunch to N registers.
+template <uint32_t N, uint32_t kLaunch>
+__device__ __forceinline__ void regs_set() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes multiples of 8 in [24, 256]");
+    if constexpr (N > kLaunch) regs_increase<N>();
+    else if constexpr (N < kLaunch) regs_decrease<N>();
 }
 
 }  // namespace dev
