@@ -158,8 +158,9 @@ struct BwdCfg {
     __device__ static uint32_t ds_off(uint32_t st) { return kDsInDo ? kOffDO + st * kTileBytes : kOffDS; }
     // Register split of the 512 threads (launch allocation 128 each):
     // gradient warpgroups, the warpgroup of single-warp roles, dQ warpgroup.
-    static constexpr uint32_t kRegsGrad = 160, kRegsMisc = 88, kRegsDq = 104;
-    static_assert(2 * kRegsGrad + kRegsMisc + kRegsDq <= 4 * 128, "register split exceeds the launch allocation");
+    static constexpr uint32_t kRegsLaunch = 128;  // 65536 / 512 threads
+    static constexpr uint32_t kRegsGrad = 144, kRegsMisc = 88, kRegsDq = 136;
+    static_assert(2 * kRegsGrad + kRegsMisc + kRegsDq <= 4 * kRegsLaunch, "register split exceeds the launch allocation");
 };
 
 // warps that read each ring entry: MMA, 8 gradient, flush, row statistics, 4 dQ
@@ -169,7 +170,9 @@ struct BwdBars {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[2], q_empty[2];    // Q tile of stage s (q_empty: committed after dK)
     uint64_t do_full[2], do_empty[2];  // dO tile of stage s (do_empty: its dQ staging was read)
-    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_empty, stg_full, mma_done;
+    uint64_t s_full, dp_full, p_full, dq_full, dq_empty, stg_full, mma_done;
+    uint64_t dst_full;      // dS^T of the current tile is in TMEM (dK may read it)
+    uint64_t ds_full;       // dS of the current tile is in shared memory (dQ may read it)
     uint64_t acc_full;      // dK, dV of the item are complete (committed after its last dK)
     uint64_t acc_empty;     // the gradient warpgroups have read dK, dV out of TMEM
     uint64_t dv_done;       // dV of the current tile has read the dO tile (dS may overwrite it)
@@ -236,13 +239,16 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 //   warps 12-15 dQ readout: TMEM -> shared staging
 // Per query tile t (in the order every role enumerates them):
 //   MMA:      [dq_empty(t-1)] dP^T(t) | [p_full(t)] dV += P^T dO -> dv_done |
-//             S^T(t+1) when the item has a next tile (S^T(first) at item start) |
-//             [ds_full(t)] dK += dS^T Q -> q_empty, dQ = dS K (into the dP^T columns)
-//   gradient: P^T(t) -> p_full | dS^T(t) (into the dO tile of t once dV has
-//             read it) -> ds_full, then straight on to P^T(t+1) (S^T(t+1) was
-//             issued while they computed dS^T(t))
-//   dQ warps: dQ(t) -> registers -> dq_empty -> staging in the dO tile of t
-//             and the staging buffer -> stg_full
+//             [dst_full(t)] dK += dS^T Q -> q_empty | S^T(t+1) when the item has a
+//             next tile (S^T(first) at item start) | [ds_full(t)] dQ = dS K (into
+//             the dP^T columns)
+//   gradient: P^T(t) -> p_full | dS^T(t) to TMEM -> dst_full, then dS(t) into
+//             the dO tile of t once dV has read it -> ds_full | P^T(t+1)
+// The order keeps the dS stores beside a TS product (dK): an SS product reads
+// 128 B of shared memory per clock and leaves other shared-memory traffic
+// little bandwidth.
+//   dQ warps: dQ(t) -> registers (all D columns) -> dq_empty -> staging in the
+//             dO tile of t and the staging buffer -> stg_full
 //   flush:    TMA reduce-adds of the staging into the fp32 accumulator; the
 //             dO tile is released (do_empty) once its boxes have been read,
 //             the staging buffer (stg_empty) once the others have.
@@ -285,6 +291,7 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(&bars.dp_full, 1);
         mbar_init(&bars.p_full, 256);
         mbar_init(&bars.ds_full, 256);
+        mbar_init(&bars.dst_full, 256);
         mbar_init(&bars.dq_full, 1);
         mbar_init(&bars.dq_empty, 128);
         mbar_init(&bars.stg_full, 128);
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(512, 1)
     const Watchdog wd{&p.ctl, &bars.abort_flag};
 
     if (warp >= 8 && warp < 12) {
-        regs_decrease<C::kRegsMisc>();
+        regs_set<C::kRegsMisc, C::kRegsLaunch>();
         if (warp == 8) {
             // ------------------------------------------------------------ producer (lane 0 issues)
             uint32_t act = 0, qt = 0;
@@ -448,12 +455,10 @@ __global__ void __launch_bounds__(512, 1)
                             umma_ts(tmem + C::kColDV, tmem + C::kColS + C::packed_col(kk), sdesc_at(dod_mn, kk * 2048),
                                     C::kIdescAcc, (j == 0 && kk == 0) ? 0u : 1u);
                         if (C::kDsInDo) umma_commit(&bars.dv_done);
-                        // S^T of the next query tile of this key tile: the P^T columns
-                        // are free once dV (issued above) has read them
-                        if (j + 1 < kg.n_q && !(ok = issue_st(qt + 1))) break;
-                        // dK += dS^T Q, then the Q tile goes back to the producer;
-                        // dQ = dS K (into the dP^T columns)
-                        if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
+                        // dK += dS^T Q as soon as dS^T is in TMEM (a TS product: the gradient
+                        // warpgroups' shared-memory stores of dS run beside it); the Q tile
+                        // then goes back to the producer
+                        if (!(ok = mbar_wait(&bars.dst_full, qt & 1, wd))) break;
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
@@ -461,6 +466,13 @@ __global__ void __launch_bounds__(512, 1)
                                     C::kIdescAcc, (j == 0 && kk == 0) ? 0u : 1u);
                         umma_commit(&bars.q_empty[st]);
                         if (j + 1 == kg.n_q) umma_commit(&bars.acc_full);
+                        // S^T of the next query tile of this key tile: the P^T columns
+                        // are free once dV (issued above) has read them
+                        if (j + 1 < kg.n_q && !(ok = issue_st(qt + 1))) break;
+                        // dQ = dS K (into the dP^T columns, read by dK just before) once
+                        // dS is in shared memory
+                        if (!(ok = mbar_wait(&bars.ds_full, qt & 1, wd))) break;
+                        tc_fence_after();
                         const uint32_t dsd = sdesc_lo(smem_base + C::ds_off(st), C::kHalfBytes);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
@@ -574,10 +586,9 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ readout
         // Lane i = q row i of the tile: dQ (fp32, D columns of the dP^T region)
-        // -> registers (64 columns at a time) -> the staging boxes; the TMEM
-        // columns are released as soon as the last columns are in registers,
-        // before waiting for the staging buffer.
-        regs_decrease<C::kRegsDq>();
+        // -> registers, all D columns before the TMEM columns are released (the
+        // next dP^T waits for them) -> the staging boxes.
+        regs_set<C::kRegsDq, C::kRegsLaunch>();
         const uint32_t i = threadIdx.x & 127u;
         const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
         uint32_t qt = 0;
@@ -602,33 +613,28 @@ __global__ void __launch_bounds__(512, 1)
                     ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, qt & 1, wd));
                     if (!ok) break;
                     tc_fence_after();
+                    uint32_t qr[D / 32][32];
+                    const uint32_t q_addr = tmem + lane_addr + C::kColDP;
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        uint32_t qr[2][32];
-                        const uint32_t q_addr = tmem + lane_addr + C::kColDP + 64 * h;
-                        tmem_ld32(q_addr, qr[0]);
-                        tmem_ld32(q_addr + 32, qr[1]);
-                        tmem_ld_wait();
-                        reg_fence(qr[0]);
-                        reg_fence(qr[1]);
-                        if (h == D / 64 - 1) {
-                            tc_fence_before();
-                            mbar_arrive(&bars.dq_empty);
-                        }
-                        if (2 * h >= C::kDoBoxes) {  // boxes 2h, 2h+1 go to the staging buffer
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(q_addr + 32 * c, qr[c]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) reg_fence(qr[c]);
+                    tc_fence_before();
+                    mbar_arrive(&bars.dq_empty);
+#pragma unroll
+                    for (int b = 0; b < D / 32; ++b) {
+                        if (b == C::kDoBoxes) {  // the remaining boxes go to the staging buffer
                             ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_empty, (qt & 1) ^ 1, wd));
                             if (!ok) break;
                         }
+                        uint8_t *srow = smem + C::stage_box_off(b, st) + i * 128;
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            uint8_t *srow = smem + C::stage_box_off(2 * h + c, st) + i * 128;
-#pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                const uint4 v = row_ok ? make_uint4(qr[c][4 * c8], qr[c][4 * c8 + 1],
-                                                                    qr[c][4 * c8 + 2], qr[c][4 * c8 + 3])
-                                                       : make_uint4(0, 0, 0, 0);
-                                *reinterpret_cast<uint4 *>(srow + ((c8 ^ (i & 7)) * 16)) = v;
-                            }
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint4 v = row_ok ? make_uint4(qr[b][4 * c8], qr[b][4 * c8 + 1], qr[b][4 * c8 + 2],
+                                                                qr[b][4 * c8 + 3])
+                                                   : make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(srow + ((c8 ^ (i & 7)) * 16)) = v;
                         }
                     }
                     if (!ok) break;
@@ -641,7 +647,7 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------------------ gradient warpgroups
         // Warpgroup w (warps 4w .. 4w+3) owns query rows / S^T columns
         // 64w .. 64w+63 of every tile and head_dim columns D/2 w .. of dK, dV.
-        regs_increase<C::kRegsGrad>();
+        regs_set<C::kRegsGrad, C::kRegsLaunch>();
         const int wg = static_cast<int>(warp >> 2);
         const uint32_t i = threadIdx.x & 127u;  // TMEM lane: key row of S^T, dP^T, dK, dV
         const uint32_t lane_addr = ((warp & 3u) * 32u) << 16;
@@ -750,39 +756,38 @@ __global__ void __launch_bounds__(512, 1)
                         tmem_ld_wait();
                         reg_fence(dr[0]);
                         reg_fence(dr[1]);
-                        uint8_t *row = smem + C::ds_off(qt % C::kQStages) + wg * C::kHalfBytes + i * 128;
+                        uint32_t pk[2][16];
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {  // q rows 64w + 32c ..
-                            uint32_t pk[16];
 #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
                                 const float2 d2 = make_float2(__uint_as_float(dr[c][e]), __uint_as_float(dr[c][e + 1]));
                                 const float2 x = __fmul2_rn(make_float2(pt[32 * c + e], pt[32 * c + e + 1]),
                                                             __fadd2_rn(d2, nd2[16 * c + e / 2]));
-                                pk[e / 2] = pack_bf16(x.x, x.y);
-                            }
-                            tmem_st16(dp_addr + c0 + 16 * c, pk);
-                            if (c == 0) {
-                                // the dS buffer is free: dV has read the dO tile it
-                                // shares, or the previous dQ has read the own buffer
-                                ok = C::kDsInDo ? mbar_wait(&bars.dv_done, qt & 1, wd)
-                                                : mbar_wait(&bars.dq_full, (qt & 1) ^ 1, wd);
-                                ok = __all_sync(0xffffffffu, ok);
-                                if (!ok) break;
-                            }
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int c8 = 4 * c + j;  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
-                                *reinterpret_cast<uint4 *>(row + ((c8 ^ (i & 7)) * 16)) =
-                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                pk[c][e / 2] = pack_bf16(x.x, x.y);
                             }
                         }
+                        tmem_st16(dp_addr + c0, pk[0]);
+                        tmem_st16(dp_addr + c0 + 16, pk[1]);
                         tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&bars.dst_full);
+                        // the dS buffer is free: dV has read the dO tile it shares, or
+                        // the previous dQ has read the own buffer
+                        ok = C::kDsInDo ? mbar_wait(&bars.dv_done, qt & 1, wd) : mbar_wait(&bars.dq_full, (qt & 1) ^ 1, wd);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (ok) {
+                            uint8_t *row = smem + C::ds_off(qt % C::kQStages) + wg * C::kHalfBytes + i * 128;
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8)  // 16-byte chunk: q rows 8 c8 .. 8 c8 + 7 of the half
+                                *reinterpret_cast<uint4 *>(row + ((c8 ^ (i & 7)) * 16)) =
+                                    make_uint4(pk[c8 >> 2][4 * (c8 & 3)], pk[c8 >> 2][4 * (c8 & 3) + 1],
+                                               pk[c8 >> 2][4 * (c8 & 3) + 2], pk[c8 >> 2][4 * (c8 & 3) + 3]);
+                        }
                     }
                     if (!ok) break;
                     mbar_arrive(&bars.row_empty[qt & 1]);  // row statistics of this tile no longer read
                     fence_view_async_shared();
-                    tc_fence_before();
                     mbar_arrive(&bars.ds_full);
                 }
             }
