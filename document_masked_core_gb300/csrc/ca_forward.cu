@@ -495,21 +495,28 @@ const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                     rescale = true;
                 }
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                float sum0 = 0.f, sum1 = 0.f;
-                uint32_t pk[2][32];
+                // paired f32x2 arithmetic: the softmax is bound by instruction issue
+                // (the two tiles' warps share each scheduler), not by the ex2 unit
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                float2 sum2 = make_float2(0.f, 0.f);
+                // P of keys 32c .. 32c+31 packed two per column into columns 16c ..: every S
+                // column is in registers already, so each chunk is stored as soon as it is
+                // ready (fewer live registers)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, -m_use));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, -m_use));
-                        sum0 += p0;
-                        sum1 += p1;
-                        pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
+                        const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                                                     sc2, nm2);
+                        const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                        sum2 = __fadd2_rn(sum2, p2);
+                        pk[e >> 1] = pack_bf16(p2.x, p2.y);
                     }
-                l = l * alpha + (sum0 + sum1);
-                tmem_st32(s_addr, pk[0]);
-                tmem_st32(s_addr + 32, pk[1]);
+                    tmem_st16(s_addr + 16 * c, pk);
+                }
+                l = l * alpha + (sum2.x + sum2.y);
                 if (i > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
