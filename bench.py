@@ -10,7 +10,9 @@ The metric counts 12 * head_dim * H_q FLOPs per causal (token, key) pair:
 Printed (rank 0, one JSON line): whole-job TFLOP/s over the timed steps with
 inputs resident in HBM (`value`), the same through the C ABI with host
 buffers (`e2e`: pinned host -> device copies of Q, K, V, dO and device -> host
-copies of dQ, dK, dV inside each timed step), the roofline of the dominant
+copies of dQ, dK, dV of every step inside the timed region, the copies of the
+next and previous steps overlapping each step's compute on their own streams;
+the one-stream serial schedule is reported beside it), the roofline of the dominant
 kernel (the backward main kernel, timed live with CUDA events on its stream),
 the clocks seen during the timed region, and the fp64 oracle timed on the host
 cores on a bounded sample of the same workload (`cpu_baseline`).
@@ -258,8 +260,16 @@ def run_reference(args, rank, world):
 
 def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_step):
     """The same step through the C ABI with host buffers: pinned host -> device
-    copies of Q, K, V, dO and device -> host copies of dQ, dK, dV inside every
-    timed step."""
+    copies of Q, K, V, dO and device -> host copies of dQ, dK, dV inside the timed
+    region, every step.
+
+    Two schedules over the same host buffers.  Serial: one stream runs each
+    step's copies in, forward, backward and copies out in turn.  Overlapped (the
+    reported value): device inputs and outputs are double-buffered, the
+    host -> device copies run on their own stream and the device -> host copies on
+    another, so step k+1's inputs arrive and step k-1's gradients leave while step
+    k computes (events keep each buffer slot from being reused early); the timed
+    region starts before the first copy in and ends after the last copy out."""
     import torch
     q, k, v, do = inputs
     o, lse = fwd_out
@@ -272,36 +282,83 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
     hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
     hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
     hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
-    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    q2, k2, v2, do2 = (torch.empty_like(x) for x in (q, k, v, do))
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-    d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
+    h_in, h_out = (hq, hk, hv, hdo), (hdq, hdk, hdv)
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    dev_in = [tuple(torch.empty_like(x) for x in (q, k, v, do)) for _ in range(2)]
+    dev_out = [tuple(torch.empty_like(x) for x in (dq, dk, dv)) for _ in range(2)]
 
-    def e2e_step():
+    def compute(slot):
+        qi, ki, vi, doi = dev_in[slot]
+        dqo, dko, dvo = dev_out[slot]
+        plan.forward(qi, ki, vi, o, lse, ws, stream=sh)
+        plan.backward(qi, ki, vi, o, lse, doi, dqo, dko, dvo, ws, stream=sh)
+
+    def serial_step():
         with torch.cuda.stream(stream):
-            for dst, src in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
+            for dst, src in zip(dev_in[0], h_in):
                 dst.copy_(src, non_blocking=True)
-            plan.forward(q2, k2, v2, o, lse, ws, stream=sh)
-            plan.backward(q2, k2, v2, o, lse, do2, dq_, dk_, dv_, ws, stream=sh)
-            for dst, src in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            compute(0)
+            for dst, src in zip(h_out, dev_out[0]):
                 dst.copy_(src, non_blocking=True)
 
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
-    stream.synchronize()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the slot's step computed (inputs free, outputs ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # the slot's outputs reached the host (outputs free)
+
+    def overlapped(n):
+        used = [False, False]
+        last = 0
+        for i in range(n):
+            slot = i % 2
+            with torch.cuda.stream(s_in):
+                if used[slot]:
+                    s_in.wait_event(ev_done[slot])
+                for dst, src in zip(dev_in[slot], h_in):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[slot].record(s_in)
+            stream.wait_event(ev_in[slot])
+            if used[slot]:
+                stream.wait_event(ev_out[slot])
+            with torch.cuda.stream(stream):
+                compute(slot)
+            ev_done[slot].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[slot])
+                for dst, src in zip(h_out, dev_out[slot]):
+                    dst.copy_(src, non_blocking=True)
+                ev_out[slot].record(s_out)
+            used[slot] = True
+            last = slot
+        stream.wait_event(ev_out[last])  # the last copy out ends the region
+
+    def timed(run):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        run()
+        end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    warm = max(1, args.warmup // 2)
+    timed(lambda: [serial_step() for _ in range(warm)])
     barrier(world)
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e2.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world)
+    serial_ms = max_over_ranks(timed(lambda: [serial_step() for _ in range(args.steps)]) / args.steps, world)
+    timed(lambda: overlapped(warm))
+    barrier(world)
+    e2e_ms = max_over_ranks(timed(lambda: overlapped(args.steps)) / args.steps, world)
     if plan.device_status(stream=sh) != 0:
         raise RuntimeError("device error in the end-to-end region")
-
     return {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "schedule": "double-buffered: copies in of step k+1 and out of step k-1 on their own streams "
+                        "during step k's compute",
+            "serial_ms_per_step": serial_ms,
+            "serial_value": flops_step * world / (serial_ms * 1e-3) / 1e12}
 
 
 def measure_masks(args, dev, stream, causal_pairs):
