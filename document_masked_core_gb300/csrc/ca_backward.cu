@@ -289,20 +289,20 @@ __global__ void __launch_bounds__(512, 1)
         }
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.p_full, 256);
-        mbar_init(&bars.ds_full, 256);
-        mbar_init(&bars.dst_full, 256);
+        mbar_init(&bars.p_full, 8);  // one arrival per warp
+        mbar_init(&bars.ds_full, 8);  // one arrival per warp
+        mbar_init(&bars.dst_full, 8);  // one arrival per warp
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_empty, 128);
-        mbar_init(&bars.stg_full, 128);
+        mbar_init(&bars.dq_empty, 4);  // one arrival per warp
+        mbar_init(&bars.stg_full, 4);  // one arrival per warp
         mbar_init(&bars.mma_done, 1);
         mbar_init(&bars.acc_full, 1);
-        mbar_init(&bars.acc_empty, 256);
+        mbar_init(&bars.acc_empty, 8);  // one arrival per warp
         mbar_init(&bars.dv_done, 1);
         mbar_init(&bars.stg_empty, 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars.row_full[b], 32);
-            mbar_init(&bars.row_empty[b], 256);
+            mbar_init(&bars.row_full[b], 1);   // one arrival per warp
+            mbar_init(&bars.row_empty[b], 8);
         }
         for (int r = 0; r < 4; ++r) {
             mbar_init(&bars.ring_full[r], 1);
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(512, 1)
                             sLse[b * 128 + lane + 32 * j] = l2[j];
                             sD[b * 128 + lane + 32 * j] = nd[j];
                         }
-                        mbar_arrive(&bars.row_full[b]);
+                        mbar_arrive_warp(&bars.row_full[b]);
                     }
                 }
             }
@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) reg_fence(qr[c]);
                     tc_fence_before();
-                    mbar_arrive(&bars.dq_empty);
+                    mbar_arrive_warp(&bars.dq_empty);
 #pragma unroll
                     for (int b = 0; b < D / 32; ++b) {
                         if (b == C::kDoBoxes) {  // the remaining boxes go to the staging buffer
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     if (!ok) break;
                     fence_view_async_shared();
-                    mbar_arrive(&bars.stg_full);
+                    mbar_arrive_warp(&bars.stg_full);
                 }
             }
         }
@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&bars.p_full);
+                    mbar_arrive_warp(&bars.p_full);
                     // ---- dS'^T = P'^T (dP^T - D) = scale dS^T: to TMEM (A of dK += dS^T Q) and
                     // to shared memory half w as the MN-major A of dQ = dS K (key row i
                     // holds q rows 64w .. 64w+63, 16-byte chunks swizzled by i % 8)
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(512, 1)
                         tmem_st16(dp_addr + c0 + 16, pk[1]);
                         tmem_st_wait();
                         tc_fence_before();
-                        mbar_arrive(&bars.dst_full);
+                        mbar_arrive_warp(&bars.dst_full);
                         // the dS buffer is free: dV has read the dO tile it shares, or
                         // the previous dQ has read the own buffer
                         ok = C::kDsInDo ? mbar_wait(&bars.dv_done, qt & 1, wd) : mbar_wait(&bars.dq_full, (qt & 1) ^ 1, wd);
@@ -786,9 +786,9 @@ __global__ void __launch_bounds__(512, 1)
                         }
                     }
                     if (!ok) break;
-                    mbar_arrive(&bars.row_empty[qt & 1]);  // row statistics of this tile no longer read
+                    mbar_arrive_warp(&bars.row_empty[qt & 1]);  // row statistics of this tile no longer read
                     fence_view_async_shared();
-                    mbar_arrive(&bars.ds_full);
+                    mbar_arrive_warp(&bars.ds_full);
                 }
             }
             if (!ok) break;
@@ -827,7 +827,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&bars.acc_empty);
+                mbar_arrive_warp(&bars.acc_empty);
             }
             ++act;
         }
