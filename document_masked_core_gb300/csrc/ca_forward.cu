@@ -257,9 +257,9 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&bars.q_full[x], 1);
             mbar_init(&bars.q_empty[x], 1);
             mbar_init(&bars.s_full[x], 1);
-            mbar_init(&bars.p_full[x], 128);
+            mbar_init(&bars.p_full[x], 4);  // one arrival per warp
             mbar_init(&bars.o_full[x], 1);
-            mbar_init(&bars.o_empty[x], 128);
+            mbar_init(&bars.o_empty[x], 4);
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
@@ -531,7 +531,7 @@ const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars.p_full[x]);
+                mbar_arrive_warp(&bars.p_full[x]);
             }
             if (!ok) break;
             // epilogue: O / l and LSE once the last PV of this tile has landed
@@ -582,7 +582,7 @@ const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.o_empty[x]);
+            mbar_arrive_warp(&bars.o_empty[x]);
             const float lse_row = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
             if (valid && split) {
                 p.split.lse[(gi.slot0 + gi.part) * 256 + rowslot] = lse_row;
