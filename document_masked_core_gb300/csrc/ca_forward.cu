@@ -82,7 +82,9 @@ struct FwdBars {
     uint64_t ring_full[4], ring_empty[4];
     int32_t ring[4];
     uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t k_full[2], v_full[2];
+    uint64_t k_empty[2];  // committed after the last S product that reads the K tile
+    uint64_t v_empty[2];  // committed after the last PV product that reads the V tile
     uint64_t s_full[2], p_full[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t mma_done;
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(320, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
         mbar_init(&bars.mma_done, 1);
         for (int r = 0; r < 4; ++r) {
@@ -318,13 +321,17 @@ __global__ void __launch_bounds__(320, 1)
                 for (int32_t i = 0; i < gi.n_kv && ok; ++i, ++kv_it) {
                     const uint32_t st = kv_it % C::kStages;
                     const uint32_t ph = (kv_it / C::kStages) & 1;
-                    if (!(ok = mbar_wait(&bars.kv_empty[st], ph ^ 1, wd))) break;
+                    // K and V stages are released separately: K once both query tiles'
+                    // S products have read it (an iteration before V), so each K load has
+                    // about two iterations to land before its S product
+                    if (!(ok = mbar_wait(&bars.k_empty[st], ph ^ 1, wd))) break;
                     const int32_t key_row = gi.kv_off + gi.kr.tile(gi.i0 + i) * kTileKeys;
                     mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
                         tma_load_3d(sK + st * C::kTileBytes + h * C::kHalfBytes, &tm_k, &bars.k_full[st], h * 64,
                                     gi.g, key_row);
+                    if (!(ok = mbar_wait(&bars.v_empty[st], ph ^ 1, wd))) break;
                     mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
@@ -341,12 +348,15 @@ __global__ void __launch_bounds__(320, 1)
             uint32_t s_it[2] = {0, 0}, q_it[2] = {0, 0}, o_it[2] = {0, 0};
             bool ok = true;
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+            int32_t nk1 = 0;  // key tiles tile B of the current item visits
             // S_x = Q_x K^T into tile x's S columns, for the key tile of ring index kvi
-            auto issue_s = [&](int x, uint32_t kvi) -> bool {
+            // (entry i of the item); tile A's product comes first, so the K tile is
+            // released after tile B's, or after A's when B does not visit it
+            auto issue_s = [&](int x, uint32_t kvi, int32_t i) -> bool {
                 const uint32_t st = kvi % C::kStages;
                 if (!mbar_wait(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
                 tc_fence_after();
-const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
+                const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
                 const uint32_t bd = sdesc_lo(k_base + st * C::kTileBytes, 16);
                 const uint32_t d_s = tmem + C::kColS + x * 128;
 #pragma unroll
@@ -355,6 +365,7 @@ const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
                     umma_ss(d_s, sdesc_at(ad, off), sdesc_at(bd, off), C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars.s_full[x]);
+                if (x == 1 || i >= nk1) umma_commit(&bars.k_empty[st]);
                 return true;
             };
             for (uint32_t r = 0; ok; ++r) {
@@ -365,12 +376,13 @@ const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
                 const ItemGeo gi = decode_item(p, idx);
                 if (gi.n_kv == 0) continue;
                 const int32_t nk[2] = {gi.t[0].n_kv, gi.t[1].n_kv};
+                nk1 = nk[1];
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     if (nk[x] == 0) continue;
                     if (!(ok = mbar_wait(&bars.q_full[x], q_it[x] & 1, wd))) break;
                     tc_fence_after();
-                    if (!(ok = issue_s(x, kv_it))) break;
+                    if (!(ok = issue_s(x, kv_it, 0))) break;
                 }
                 for (int32_t i = 0; i < gi.n_kv && ok; ++i) {
                     const uint32_t kvi = kv_it + i;
@@ -382,7 +394,7 @@ const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
                         if (!(ok = mbar_wait(&bars.p_full[x], s_it[x] & 1, wd))) break;
                         if (i == 0 && !(ok = mbar_wait(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
                         tc_fence_after();
-const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
+                        const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                         const uint32_t d_o = tmem + C::kColO + x * D, a_p = tmem + C::kColS + x * 128;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
@@ -390,7 +402,7 @@ const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                                     (i > 0 || kk > 0) ? 1u : 0u);
                         ++s_it[x];
                         if (i + 1 < nk[x]) {
-                            if (!(ok = issue_s(x, kvi + 1))) break;
+                            if (!(ok = issue_s(x, kvi + 1, i + 1))) break;
                         } else {
                             umma_commit(&bars.o_full[x]);   // O_x complete
                             umma_commit(&bars.q_empty[x]);  // Q_x no longer read
@@ -399,7 +411,7 @@ const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&bars.kv_empty[st]);
+                    umma_commit(&bars.v_empty[st]);
                 }
                 kv_it += gi.n_kv;
             }
