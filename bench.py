@@ -37,6 +37,7 @@ import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0  # GB300 nominal dense bf16 (without 2:4 sparsity)
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -637,7 +638,12 @@ def run_gpu(args, rank, world, local):
                 "plan_ms": plan_ms,
             },
             "pct_of_peak": {"burst": 100.0 * value / world / peak, "sustained": 100.0 * value / world / peak_sus,
-                            "peaks": pk_kind},
+                            "peaks": pk_kind,
+                            "nominal_dense": 100.0 * value / world / NOMINAL_DENSE_BF16_TFLOPS,
+                            "nominal_note": "vs the nominal 2.25 PFLOP/s dense bf16 of a GB300 (context only)"},
+            "tflops_14d_convention": {"value": value * 14.0 / 12.0,
+                                      "note": "FlashAttention's 2.5x backward convention (14 d per pair); "
+                                              "not the headline, which counts 12 d"},
             "parts_ms": {"forward": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
                          "bwd_dq_finalize": fin_ms},
             "parts_tflops": {"forward": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12,
