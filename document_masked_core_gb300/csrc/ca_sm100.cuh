@@ -62,6 +62,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test with a suspend-time hint (ns): a waiting warp sleeps until the
+// phase completes or the hint runs out instead of re-polling the barrier, which
+// leaves the shared-memory pipe to the roles that are working.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Per-CTA abort state: once any wait of the CTA runs out, every later wait
 // returns false at once so all roles drain and reach the final barrier.
 struct Watchdog {
@@ -77,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*wd.abort_flag) return false;
         if (globaltimer() - t0 > wd.ctl->wait_limit_ns) {
             *wd.abort_flag = 1u;
