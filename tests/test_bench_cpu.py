@@ -52,3 +52,29 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu capture only while the
+    kernel sources it lists still hash to the recorded value."""
+    import hashlib
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    name = "traffic_bwd_main_llama8b_chunk_64k.json"
+    with open(os.path.join(ROOT, "profiles", name)) as f:
+        d = json.load(f)
+    (tmp_path / "profiles").mkdir()
+    h = hashlib.sha256()
+    for src in d["sources"]:
+        dst = tmp_path / src
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(ROOT, src), dst)
+        h.update(dst.read_bytes())
+    d["sources_sha256"] = h.hexdigest()
+    (tmp_path / "profiles" / name).write_text(json.dumps(d))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic() == int(d["dram_read_bytes"]) + int(d["dram_write_bytes"])
+    changed = tmp_path / d["sources"][0]
+    changed.write_bytes(changed.read_bytes() + b"\n")
+    assert bench.measured_traffic() is None
