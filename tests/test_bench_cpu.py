@@ -34,7 +34,7 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_max_time():
     port = free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(2, port, out), nprocs=2, start_method="spawn")
         assert dict(out) == {0: 11.0, 1: 11.0}

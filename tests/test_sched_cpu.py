@@ -340,7 +340,7 @@ def _rank(rank, world, port, docs, out):
 def test_two_gloo_ranks_share_one_schedule():
     docs = doc_sets()["llama8b_64k"]
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(2, port, docs, out), nprocs=2, start_method="spawn")
         res = dict(out)
