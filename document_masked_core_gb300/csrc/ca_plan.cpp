@@ -273,7 +273,7 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     for (int32_t i = 0; i < n_docs; ++i) {
         if (doc_len[i] < 1 || doc_kv_offset[i] < 0)
             return fail(CA_ERR_INVALID_ARG, "document " + std::to_string(i) + " has a bad length or offset");
-        if (doc_len[i] > kI32Max || doc_kv_offset[i] + doc_len[i] > kI32Max)
+        if (doc_len[i] > kI32Max || doc_kv_offset[i] > kI32Max - doc_len[i])  // no int64 overflow
             return fail(CA_ERR_INVALID_ARG, "document rows must stay below 2^31");
         ranges[i] = {doc_kv_offset[i], doc_kv_offset[i] + doc_len[i]};
         total_kv = std::max(total_kv, doc_kv_offset[i] + doc_len[i]);
@@ -307,8 +307,9 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
         const int64_t L = doc_len[T.doc_id];
         if (T.q_len < 1 || T.kv_len < 1) return fail(CA_ERR_INVALID_ARG, tn + "q_len and kv_len must be >= 1");
         if (T.q_start < 0 || T.kv_start < 0) return fail(CA_ERR_INVALID_ARG, tn + "negative start");
-        if (T.q_start + T.q_len > L) return fail(CA_ERR_INVALID_ARG, tn + "query shard runs past the document");
-        if (T.kv_start + T.kv_len > L) return fail(CA_ERR_INVALID_ARG, tn + "KV block runs past the document");
+        // written as L - len so that no int64 sum can overflow (L <= 2^31 - 1, len >= 1)
+        if (T.q_start > L - T.q_len) return fail(CA_ERR_INVALID_ARG, tn + "query shard runs past the document");
+        if (T.kv_start > L - T.kv_len) return fail(CA_ERR_INVALID_ARG, tn + "KV block runs past the document");
         if (row0 + T.q_len > kI32Max) return fail(CA_ERR_INVALID_ARG, "total query rows must stay below 2^31");
         DevTask &d = p->h_tasks[t];
         d.row0 = static_cast<int32_t>(row0);
@@ -566,6 +567,8 @@ ca_status_t ca_merge(int32_t n_parts, const void *const *o_parts, const float *c
     if (!o_parts || !lse_parts || !o_out) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
     if (rows < 0 || heads < 1 || head_dim < 8 || head_dim > 256 || head_dim % 8 != 0)
         return fail(CA_ERR_INVALID_ARG, "bad rows / heads / head_dim");
+    if (rows > (int64_t(1) << 50) / (int64_t(heads) * head_dim))  // the launch sizes in int64
+        return fail(CA_ERR_INVALID_ARG, "rows * heads * head_dim exceeds 2^50 elements");
     if ((parts_dtype != CA_DTYPE_BF16 && parts_dtype != CA_DTYPE_FP32) ||
         (out_dtype != CA_DTYPE_BF16 && out_dtype != CA_DTYPE_FP32))
         return fail(CA_ERR_INVALID_ARG, "bad dtype");

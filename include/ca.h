@@ -249,7 +249,9 @@ ca_status_t ca_backward_noalloc(const ca_plan_t *plan, const void *q, const void
  * pointers (1 <= n_parts <= 64); each o part is [rows, heads, head_dim] of
  * parts_dtype, each lse part [rows, heads] float32.  o_out is
  * [rows, heads, head_dim] of out_dtype; lse_out may be NULL.  head_dim must
- * be a multiple of 8 and at most 256.
+ * be a multiple of 8 and at most 256, and rows * heads * head_dim at most
+ * 2^50; other sizes, NULL or unaligned pointers give CA_ERR_INVALID_ARG
+ * before anything is launched.
  */
 ca_status_t ca_merge(int32_t n_parts, const void *const *o_parts, const float *const *lse_parts,
                      int32_t parts_dtype, int64_t rows, int32_t heads, int32_t head_dim,

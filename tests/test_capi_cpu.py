@@ -160,6 +160,11 @@ def test_invalid_descriptors_rejected():
         dict(num_q_heads=6, num_kv_heads=4),    # not a multiple
         dict(doc_len=[10, 5], doc_kv_offset=[0, 8]),  # overlapping documents
         dict(softmax_scale=-1.0),
+        # sums that would overflow int64 if the host formed them
+        dict(task_q_start=[2 ** 63 - 5]),
+        dict(task_kv_start=[2 ** 63 - 5]),
+        dict(doc_kv_offset=[2 ** 63 - 5]),
+        dict(task_q_len=[2 ** 63 - 1]),
     ]
     for b in bad:
         kw = dict(base, **b)
@@ -170,3 +175,13 @@ def test_invalid_descriptors_rejected():
         with pytest.raises(ca.CAError) as ei:
             ca.dry_run(**dict(base, **b))
         assert ei.value.status == capi.CA_ERR_UNSUPPORTED, b
+
+
+def test_merge_rejects_sizes_that_overflow_the_launch():
+    """ca_merge validates its sizes on the host before any CUDA call."""
+    with pytest.raises(ca.CAError) as ei:
+        capi.merge([16], [16], 2 ** 62, 1, 64, 16, stream=0)
+    assert ei.value.status == capi.CA_ERR_INVALID_ARG
+    with pytest.raises(ca.CAError) as ei:
+        capi.merge([16], [16], 4, 1, 60, 16, stream=0)  # head_dim not a multiple of 8
+    assert ei.value.status == capi.CA_ERR_INVALID_ARG
