@@ -144,6 +144,7 @@ void free_device(ca_plan *p) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int64_t kI32Max = 2147483647LL;
+constexpr int32_t kMaxQHeads = 4096;  // keeps every per-row index product far inside int64
 
 }  // namespace
 
@@ -258,6 +259,7 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     const ca_shape_t sh = *shape;
     if (sh.num_q_heads < 1 || sh.num_kv_heads < 1 || sh.num_q_heads % sh.num_kv_heads != 0)
         return fail(CA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+    if (sh.num_q_heads > kMaxQHeads) return fail(CA_ERR_UNSUPPORTED, "num_q_heads must be at most 4096");
     if (!(sh.softmax_scale > 0.f) || !std::isfinite(sh.softmax_scale))
         return fail(CA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
     if (sh.o_dtype != CA_DTYPE_BF16 && sh.o_dtype != CA_DTYPE_FP32)
@@ -338,6 +340,7 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     p->total_q = row0;
 
     build_fwd_items(p, &hp->fwd);
+    if (p->n_fwd > kI32Max) return fail(CA_ERR_UNSUPPORTED, "the forward work list exceeds 2^31 items");
 
     // documents -> tasks (CSR), and backward tiles: (document, kv head, key tile)
     std::vector<int32_t> &ptr = hp->ptr, &dtasks = hp->dtasks, &doc_info = hp->doc_info;
@@ -383,9 +386,22 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
         });
     }
     p->n_bwd = static_cast<int64_t>(bwd.size());
+    if (p->n_bwd > kI32Max) return fail(CA_ERR_UNSUPPORTED, "the backward work list exceeds 2^31 items");
 
     set_workspace_bytes(p);
     return CA_OK;
+}
+
+// build_host_plan behind the C boundary: a failed host allocation becomes a
+// status instead of an exception leaving an extern "C" function.
+ca_status_t build_host_plan_guarded(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
+                                    const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
+                                    const ca_shape_t *shape, HostPlan *hp) {
+    try {
+        return build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, hp);
+    } catch (const std::bad_alloc &) {
+        return fail(CA_ERR_INVALID_ARG, "host memory exhausted while planning");
+    }
 }
 
 }  // namespace
@@ -437,7 +453,7 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
                                    const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs) {
     if (!info) return fail(CA_ERR_INVALID_ARG, "info is NULL");
     HostPlan hp;
-    ca_status_t st = build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st = build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
     if (st == CA_OK) {
         fill_info(hp.p, info);
         if (task_pairs) std::copy(hp.p->task_pairs.begin(), hp.p->task_pairs.end(), task_pairs);
@@ -464,7 +480,7 @@ ca_status_t ca_plan_create_masked(const ca_task_t *tasks, const ca_mask_t *masks
     if (!out) return fail(CA_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     HostPlan hp;
-    ca_status_t st = build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st = build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
     if (st != CA_OK) {
         delete hp.p;
         return st;

@@ -101,9 +101,11 @@ typedef struct {
  * Errors: CA_ERR_INVALID_ARG for n_tasks < 1, n_docs < 1, q_len < 1,
  * kv_len < 1, q_start < 0, kv_start < 0, q_start + q_len > doc_len,
  * kv_start + kv_len > doc_len, unknown doc_id, overlapping document ranges,
- * H_q % H_kv != 0, non-positive or non-finite scale, token counts >= 2^31;
- * CA_ERR_UNSUPPORTED for head_dim not in {64, 128} or H_q / H_kv not a
- * divisor of 128.  *out is set only on CA_OK; free with ca_plan_destroy.
+ * H_q % H_kv != 0, non-positive or non-finite scale, token counts >= 2^31,
+ * host memory exhausted while planning; CA_ERR_UNSUPPORTED for head_dim not
+ * in {64, 128}, H_q / H_kv not a divisor of 128, H_q > 4096, or a work list
+ * of 2^31 items or more.  *out is set only on CA_OK; free with
+ * ca_plan_destroy.
  */
 ca_status_t ca_plan_create(const ca_task_t *tasks, int32_t n_tasks,
                            const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,

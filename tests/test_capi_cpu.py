@@ -171,7 +171,7 @@ def test_invalid_descriptors_rejected():
         with pytest.raises(ca.CAError) as ei:
             ca.dry_run(**kw)
         assert ei.value.status == capi.CA_ERR_INVALID_ARG, b
-    for b in (dict(head_dim=96), dict(num_q_heads=3, num_kv_heads=1)):
+    for b in (dict(head_dim=96), dict(num_q_heads=3, num_kv_heads=1), dict(num_q_heads=8192, num_kv_heads=64)):
         with pytest.raises(ca.CAError) as ei:
             ca.dry_run(**dict(base, **b))
         assert ei.value.status == capi.CA_ERR_UNSUPPORTED, b
