@@ -7,6 +7,7 @@
 // include/ca_sched.h.
 #include <algorithm>
 #include <cmath>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -32,8 +33,8 @@ struct ca_profile {
 
 extern "C" {
 
-ca_status_t ca_profile_create(const int64_t *nq_grid, int32_t n_nq, const int64_t *nkv_grid, int32_t n_nkv,
-                              const double *seconds, double flops_per_pair, ca_profile_t **out) {
+static ca_status_t profile_create_impl(const int64_t *nq_grid, int32_t n_nq, const int64_t *nkv_grid, int32_t n_nkv,
+                                      const double *seconds, double flops_per_pair, ca_profile_t **out) {
     using ca::fail;
     if (!out) return fail(CA_ERR_INVALID_ARG, "ca_profile_create: out is NULL");
     *out = nullptr;
@@ -63,6 +64,17 @@ ca_status_t ca_profile_create(const int64_t *nq_grid, int32_t n_nq, const int64_
         }
     *out = p;
     return CA_OK;
+}
+
+// Each entry point that builds host containers returns a failed allocation
+// as a status instead of letting the exception leave an extern "C" function.
+ca_status_t ca_profile_create(const int64_t *nq_grid, int32_t n_nq, const int64_t *nkv_grid, int32_t n_nkv,
+                              const double *seconds, double flops_per_pair, ca_profile_t **out) {
+    try {
+        return profile_create_impl(nq_grid, n_nq, nkv_grid, n_nkv, seconds, flops_per_pair, out);
+    } catch (const std::bad_alloc &) {
+        return ca::fail(CA_ERR_INVALID_ARG, "ca_profile_create: host memory exhausted");
+    }
 }
 
 ca_status_t ca_profile_predict(const ca_profile_t *prof, int64_t n_q, int64_t n_kv, double *seconds) {
@@ -147,8 +159,8 @@ struct Item {
 
 }  // namespace
 
-extern "C" ca_status_t ca_schedule(const int64_t *doc_len, int32_t n_docs, const ca_sched_params_t *params,
-                                   ca_sched_task_t *tasks_out, int64_t max_tasks, ca_sched_result_t *result) {
+static ca_status_t schedule_impl(const int64_t *doc_len, int32_t n_docs, const ca_sched_params_t *params,
+                                 ca_sched_task_t *tasks_out, int64_t max_tasks, ca_sched_result_t *result) {
     using ca::fail;
     if (!doc_len || !params || !result || n_docs < 1) return fail(CA_ERR_INVALID_ARG, "ca_schedule: NULL or empty input");
     const ca_sched_params_t &P = *params;
@@ -295,8 +307,17 @@ extern "C" ca_status_t ca_schedule(const int64_t *doc_len, int32_t n_docs, const
     return CA_OK;
 }
 
-extern "C" ca_status_t ca_shard_2n(const int64_t *doc_len, int32_t n_docs, int32_t n_ranks, ca_sched_task_t *tasks_out,
-                                   int64_t max_tasks, int64_t *n_tasks_out) {
+extern "C" ca_status_t ca_schedule(const int64_t *doc_len, int32_t n_docs, const ca_sched_params_t *params,
+                                   ca_sched_task_t *tasks_out, int64_t max_tasks, ca_sched_result_t *result) {
+    try {
+        return schedule_impl(doc_len, n_docs, params, tasks_out, max_tasks, result);
+    } catch (const std::bad_alloc &) {
+        return ca::fail(CA_ERR_INVALID_ARG, "ca_schedule: host memory exhausted");
+    }
+}
+
+static ca_status_t shard_2n_impl(const int64_t *doc_len, int32_t n_docs, int32_t n_ranks, ca_sched_task_t *tasks_out,
+                                 int64_t max_tasks, int64_t *n_tasks_out) {
     using ca::fail;
     if (!doc_len || !n_tasks_out || n_docs < 1) return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: NULL or empty input");
     if (n_ranks < 1) return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: n_ranks must be >= 1");
@@ -328,4 +349,13 @@ extern "C" ca_status_t ca_shard_2n(const int64_t *doc_len, int32_t n_docs, int32
         return fail(CA_ERR_INVALID_ARG, "ca_shard_2n: task buffer too small (" + std::to_string(*n_tasks_out) + " needed)");
     std::copy(out.begin(), out.end(), tasks_out);
     return CA_OK;
+}
+
+extern "C" ca_status_t ca_shard_2n(const int64_t *doc_len, int32_t n_docs, int32_t n_ranks, ca_sched_task_t *tasks_out,
+                                   int64_t max_tasks, int64_t *n_tasks_out) {
+    try {
+        return shard_2n_impl(doc_len, n_docs, n_ranks, tasks_out, max_tasks, n_tasks_out);
+    } catch (const std::bad_alloc &) {
+        return ca::fail(CA_ERR_INVALID_ARG, "ca_shard_2n: host memory exhausted");
+    }
 }
