@@ -297,10 +297,19 @@ class Plan:
         return out
 
     def forward(self, q, k, v, o, lse, workspace=None, stream=None):
+        """ca_forward: O and LSE of every task row.  q [total_q, H_q, d] and
+        k, v [total_kv, H_kv, d] are bf16 CUDA tensors; o [total_q, H_q, d] is
+        bf16 or float32 as the plan's o_dtype; lse [total_q, H_q] float32;
+        workspace holds at least info()["workspace_bytes"] bytes.  Runs on
+        ``stream`` (default: torch's current stream); nothing is allocated."""
         _check(load().ca_forward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
                                  _stream(stream)))
 
     def backward(self, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=None):
+        """ca_backward: dQ, dK, dV from the forward's O and LSE and the
+        upstream gradient d_o (bf16, shaped like q).  dq is shaped like q, dk
+        and dv like k (bf16); dk and dv are overwritten with the sum over every
+        task of the document (rows no task sees get 0)."""
         _check(load().ca_backward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _stream(stream)))
 
