@@ -184,6 +184,17 @@ void set_error(const std::string &msg);
 ca_status_t fail(ca_status_t st, const std::string &msg);
 ca_status_t cuda_fail(cudaError_t e, const char *what);
 
+// CA_ERR_INVALID_ARG unless the plan's device is current (its tables, error
+// word and the tensor maps of a launch live there).
+ca_status_t check_plan_device(const ca_plan *p);
+
+// Backward argument checks shared by ca_backward and ca_backward_noalloc:
+// non-NULL, 16-byte aligned, and no output (dq, dk, dv, the scratch of
+// scratch_bytes) sharing a byte with another output or with an input.
+ca_status_t check_backward_args(const ca_plan *p, const void *q, const void *k, const void *v, const void *o,
+                                const void *lse, const void *d_o, const void *dq, const void *dk, const void *dv,
+                                const void *scratch, int64_t scratch_bytes);
+
 // Builds a 3D tensor map over a [rows, heads, dim] token-major bf16 (or fp32)
 // tensor with a box of (128 bytes of dim, box_heads, box_rows) and 128-byte
 // swizzle.

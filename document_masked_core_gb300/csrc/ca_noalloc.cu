@@ -15,8 +15,9 @@
 
 namespace {
 
-// 16 MiB: enough for total_q * num_q_heads * (head_dim + 1) * 4 bytes of
-// about 32 K (row, head) pairs at head_dim 128.
+// 16 MiB: the backward's scratch is total_q * num_q_heads * (head_dim + 1)
+// * 4 bytes (each part rounded up to 256) plus 256 bytes of counters: about
+// 32 K (row, head) pairs at head_dim 128.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
@@ -25,8 +26,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" ca_status_t ca_backward_noalloc(const ca_plan_t *p, const void *q, const void *k, const void *v,
@@ -34,13 +33,11 @@ extern "C" ca_status_t ca_backward_noalloc(const ca_plan_t *p, const void *q, co
                                            void *dv, void *stream) {
     using namespace ca;
     if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
-    if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
-    const void *ptrs[] = {q, k, v, o, lse, d_o, dq, dk, dv};
-    for (const void *x : ptrs)
-        if (!aligned16(x)) return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    if (dq == dk || dq == dv || dk == dv) return fail(CA_ERR_INVALID_ARG, "gradient outputs alias");
-    if (static_cast<size_t>(p->workspace_bytes) > kNoAllocScratchBytes)
-        return fail(CA_ERR_UNSUPPORTED, "this plan needs " + std::to_string(p->workspace_bytes) +
+    // The backward touches the workspace up to the split-KV forward scratch:
+    // the fp32 dQ accumulator, the D vector and the work-queue counters.
+    const int64_t need = p->split_ws_off;
+    if (need > static_cast<int64_t>(kNoAllocScratchBytes))
+        return fail(CA_ERR_UNSUPPORTED, "this plan's backward needs " + std::to_string(need) +
                                             " bytes of scratch; ca_backward_noalloc has " +
                                             std::to_string(kNoAllocScratchBytes) +
                                             " (use ca_backward with a caller workspace)");
@@ -49,12 +46,18 @@ extern "C" ca_status_t ca_backward_noalloc(const ca_plan_t *p, const void *q, co
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev != p->device) return fail(CA_ERR_INVALID_ARG, "the plan was created on another device");
     if (dev < 0 || dev >= kMaxDevices) return fail(CA_ERR_UNSUPPORTED, "device ordinal out of range");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     void *scratch = nullptr;
     {
-        // one-time set-up per device, with that device current: the host-side
-        // name of the array is not a device address, so look the address up
+        // Set-up per device, with that device current: the host-side name of
+        // the array is not a device address, so look the address up.  Outside
+        // a stream capture it is looked up on every call (a cudaDeviceReset
+        // reloads the module and may move the array); inside a capture the
+        // address of the last call outside one is used.
         std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (!g_scratch_addr[dev]) {
+        if (cap == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
             void *addr = nullptr;
             e = cudaGetSymbolAddress(&addr, g_bwd_scratch);
             if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the backward scratch");
@@ -62,8 +65,11 @@ extern "C" ca_status_t ca_backward_noalloc(const ca_plan_t *p, const void *q, co
         }
         scratch = g_scratch_addr[dev];
     }
-    // the preprocess kernel of the backward zeroes the dQ accumulator and
-    // rewrites D, so the array's previous contents never leak into a result
+    const ca_status_t st = check_backward_args(p, q, k, v, o, lse, d_o, dq, dk, dv, scratch, need);
+    if (st != CA_OK) return st;
+    // the preprocess kernel of the backward zeroes the dQ accumulator and the
+    // work-queue counter and rewrites D, so the array's previous contents
+    // never leak into a result
     e = launch_backward(p, q, k, v, o, lse, d_o, dq, dk, dv, scratch, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward (no-allocation) launch");
     return CA_OK;

@@ -83,6 +83,50 @@ ca_status_t cuda_fail(cudaError_t e, const char *what) {
     return CA_ERR_CUDA;
 }
 
+ca_status_t check_plan_device(const ca_plan *p) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != p->device)
+        return fail(CA_ERR_INVALID_ARG, "the plan was created on device " + std::to_string(p->device) +
+                                            " but device " + std::to_string(dev) + " is current");
+    return CA_OK;
+}
+
+ca_status_t check_backward_args(const ca_plan *p, const void *q, const void *k, const void *v, const void *o,
+                                const void *lse, const void *d_o, const void *dq, const void *dk, const void *dv,
+                                const void *scratch, int64_t scratch_bytes) {
+    const void *in[] = {q, k, v, o, lse, d_o};
+    const void *out[] = {dq, dk, dv, scratch};
+    for (const void *x : in)
+        if (!x) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    for (const void *x : out)
+        if (!x) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    for (const void *x : in)
+        if (reinterpret_cast<uintptr_t>(x) & 15u) return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    for (const void *x : out)
+        if (reinterpret_cast<uintptr_t>(x) & 15u) return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    const int64_t q_b = p->total_q * p->hq * p->d * 2, kv_b = p->total_kv * p->hkv * p->d * 2;
+    const int64_t o_b = p->total_q * p->hq * p->d * (p->o_dtype == CA_DTYPE_FP32 ? 4 : 2);
+    const int64_t lse_b = p->total_q * p->hq * 4;
+    const int64_t in_n[] = {q_b, kv_b, kv_b, o_b, lse_b, q_b};
+    const int64_t out_n[] = {q_b, kv_b, kv_b, scratch_bytes};
+    auto overlaps = [](const void *a, int64_t na, const void *b, int64_t nb) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return na > 0 && nb > 0 && x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+    };
+    // outputs (dq, dk, dv, the scratch) must not share a byte with each other or with an input
+    for (int i = 0; i < 4; ++i) {
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(out[i], out_n[i], out[j], out_n[j]))
+                return fail(CA_ERR_INVALID_ARG, "output buffers overlap");
+        for (int j = 0; j < 6; ++j)
+            if (overlaps(out[i], out_n[i], in[j], in_n[j]))
+                return fail(CA_ERR_INVALID_ARG, "an output buffer overlaps an input");
+    }
+    return CA_OK;
+}
+
 ca_status_t make_tmap_3d(CUtensorMap *map, const void *base, int64_t rows, int32_t heads, int32_t dim,
                          int32_t box_heads, int32_t box_rows, bool fp32) {
     std::call_once(g_encode_once, [] {
@@ -145,6 +189,28 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr int64_t kI32Max = 2147483647LL;
 constexpr int32_t kMaxQHeads = 4096;  // keeps every per-row index product far inside int64
+constexpr int32_t kDryRunSms = 152;   // SM count assumed without a device (a GB300)
+
+// Whether byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    if (na <= 0 || nb <= 0) return false;
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
+// Byte sizes of a plan's tensors (every count is bounded far inside int64 by
+// the planning limits).
+struct BufferSizes {
+    int64_t q, kv, o, lse;
+};
+BufferSizes buffer_sizes(const ca_plan *p) {
+    BufferSizes b;
+    b.q = p->total_q * p->hq * p->d * 2;
+    b.kv = p->total_kv * p->hkv * p->d * 2;
+    b.o = p->total_q * p->hq * p->d * (p->o_dtype == CA_DTYPE_FP32 ? 4 : 2);
+    b.lse = p->total_q * p->hq * 4;
+    return b;
+}
 
 }  // namespace
 
@@ -180,24 +246,34 @@ void set_workspace_bytes(ca_plan *p) {
     p->workspace_bytes = p->split_ws_off + split_bytes;
 }
 
-// Forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1),
-// longest first; the second tile is absent past the task's last tile.  The
-// pair visits the key tiles of key_tile_ranges over both tiles' rows (each
-// tile a prefix of that sequence).  A pair with more visits than the split
-// size is cut into nparts balanced items over [i0, i1) of its sequence.
-// Split size: kv_split > 0 as given; kv_split < 0 never; kv_split = 0
-// (automatic) only when the launch has fewer than 4 waves of items on a
-// 152-SM GPU: then total visits / 152 clamped to [64, 128] key tiles per
-// part (measured on decode batches of 1 to 32 sequences of 128K tokens).
-void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
-    std::vector<FwdItem> &fwd = *out;
+// Forward items: (task, kv head, pair of consecutive query tiles 2t, 2t+1).
+// The second tile is absent past the task's last tile.  The pair visits the
+// key tiles of key_tile_ranges over both tiles' rows (each tile a prefix of
+// that sequence).  A pair with more visits than the split size is cut into
+// nparts balanced items over [i0, i1) of its sequence.  Split size:
+// kv_split > 0 as given; kv_split < 0 never; kv_split = 0 (automatic) only
+// when the launch has fewer than 4 waves of items on num_sms SMs: then total
+// visits / num_sms clamped to [64, 128] key tiles per part (measured on
+// decode batches of 1 to 32 sequences of 128K tokens).
+//
+// Order: items of one (document, kv head) are consecutive, so the CTAs that
+// run at the same time read the same K/V prefix and it stays in L2; groups
+// with the most key-tile visits first, longest items first inside a group,
+// so the launch still ends on the shortest items.
+struct FwdList {
+    std::vector<FwdItem> items;
+    int64_t n_split = 0, n_slots = 0, fwd_tile_pairs = 0;
+};
+
+void build_fwd_items(const ca_plan *p, int32_t kv_split, int32_t num_sms, FwdList *out) {
+    std::vector<FwdItem> &fwd = out->items;
     fwd.clear();
+    out->n_split = out->n_slots = out->fwd_tile_pairs = 0;
     struct Pair {
         int32_t t, tile, na, nb, n;
     };
     std::vector<Pair> pairs;
     int64_t total_visits = 0;
-    p->fwd_tile_pairs = 0;
     for (int32_t t = 0; t < p->n_tasks; ++t) {
         const DevTask &d = p->h_tasks[t];
         const int32_t ntiles = (d.q_len + p->tpt - 1) / p->tpt;
@@ -211,26 +287,24 @@ void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
             const int32_t nb = has_b ? visits_upto(r, d, end1) : 0;
             pairs.push_back({t, tile, na, nb, std::max(na, nb)});
             total_visits += static_cast<int64_t>(std::max(na, nb)) * p->hkv;
-            p->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
+            out->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;
         }
     }
-    constexpr int64_t kWaveUnits = 4 * 152;
+    const int64_t sms = std::max<int32_t>(1, num_sms);
     int64_t chunk = 0;  // 0 = no split
-    if (p->kv_split > 0) {
-        chunk = p->kv_split;
-    } else if (p->kv_split == 0 && static_cast<int64_t>(pairs.size()) * p->hkv < kWaveUnits) {
-        chunk = std::min<int64_t>(128, std::max<int64_t>(64, (total_visits + 151) / 152));
+    if (kv_split > 0) {
+        chunk = kv_split;
+    } else if (kv_split == 0 && static_cast<int64_t>(pairs.size()) * p->hkv < 4 * sms) {
+        chunk = std::min<int64_t>(128, std::max<int64_t>(64, (total_visits + sms - 1) / sms));
     }
-    p->n_split = 0;
-    p->n_slots = 0;
     for (const Pair &pr : pairs) {
         const int32_t nparts = (chunk > 0 && pr.n > chunk) ? static_cast<int32_t>((pr.n + chunk - 1) / chunk) : 1;
         for (int32_t g = 0; g < p->hkv; ++g) {
             int32_t split = -1, slot0 = 0;
             if (nparts > 1) {
-                split = static_cast<int32_t>(p->n_split++);
-                slot0 = static_cast<int32_t>(p->n_slots);
-                p->n_slots += nparts;
+                split = static_cast<int32_t>(out->n_split++);
+                slot0 = static_cast<int32_t>(out->n_slots);
+                out->n_slots += nparts;
             }
             for (int32_t part = 0; part < nparts; ++part) {
                 const int32_t i0 = static_cast<int32_t>(static_cast<int64_t>(pr.n) * part / nparts);
@@ -239,20 +313,41 @@ void build_fwd_items(ca_plan *p, std::vector<FwdItem> *out) {
             }
         }
     }
-    std::stable_sort(fwd.begin(), fwd.end(), [](const FwdItem &a, const FwdItem &b) { return a.n_kv > b.n_kv; });
-    p->n_fwd = static_cast<int64_t>(fwd.size());
+    std::vector<int64_t> group_work(static_cast<size_t>(p->n_docs) * p->hkv, 0);
+    auto group = [&](const FwdItem &a) {
+        return static_cast<size_t>(p->h_tasks[a.task].doc) * p->hkv + a.g;
+    };
+    for (const FwdItem &a : fwd) group_work[group(a)] += a.n_kv;
+    std::stable_sort(fwd.begin(), fwd.end(), [&](const FwdItem &a, const FwdItem &b) {
+        const size_t ga = group(a), gb = group(b);
+        if (ga != gb) {
+            if (group_work[ga] != group_work[gb]) return group_work[ga] > group_work[gb];
+            return ga < gb;
+        }
+        return a.n_kv > b.n_kv;
+    });
+}
+
+// Installs a forward list's counts in the plan (the items go to the device
+// separately).
+void apply_fwd_counts(ca_plan *p, const FwdList &f) {
+    p->n_fwd = static_cast<int64_t>(f.items.size());
+    p->n_split = f.n_split;
+    p->n_slots = f.n_slots;
+    p->fwd_tile_pairs = f.fwd_tile_pairs;
 }
 
 struct HostPlan {
     ca_plan *p = nullptr;
-    std::vector<FwdItem> fwd;
+    FwdList fwd;
     std::vector<BwdItem> bwd;
     std::vector<int32_t> ptr, dtasks, doc_info;
 };
 
 // Validation and all integer work of a plan; touches no device.
 ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks, const int64_t *doc_len,
-                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape, HostPlan *hp) {
+                            const int64_t *doc_kv_offset, int32_t n_docs, const ca_shape_t *shape, int32_t num_sms,
+                            HostPlan *hp) {
     if (!tasks || !doc_len || !doc_kv_offset || !shape) return fail(CA_ERR_INVALID_ARG, "NULL argument");
     if (n_tasks < 1) return fail(CA_ERR_INVALID_ARG, "n_tasks must be >= 1");
     if (n_docs < 1) return fail(CA_ERR_INVALID_ARG, "n_docs must be >= 1");
@@ -339,7 +434,9 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
     }
     p->total_q = row0;
 
-    build_fwd_items(p, &hp->fwd);
+    p->num_sms = num_sms;
+    build_fwd_items(p, p->kv_split, num_sms, &hp->fwd);
+    apply_fwd_counts(p, hp->fwd);
     if (p->n_fwd > kI32Max) return fail(CA_ERR_UNSUPPORTED, "the forward work list exceeds 2^31 items");
 
     // documents -> tasks (CSR), and backward tiles: (document, kv head, key tile)
@@ -396,12 +493,38 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
 // status instead of an exception leaving an extern "C" function.
 ca_status_t build_host_plan_guarded(const ca_task_t *tasks, const ca_mask_t *masks, int32_t n_tasks,
                                     const int64_t *doc_len, const int64_t *doc_kv_offset, int32_t n_docs,
-                                    const ca_shape_t *shape, HostPlan *hp) {
+                                    const ca_shape_t *shape, int32_t num_sms, HostPlan *hp) {
     try {
-        return build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, hp);
+        return build_host_plan(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, num_sms, hp);
     } catch (const std::bad_alloc &) {
         return fail(CA_ERR_INVALID_ARG, "host memory exhausted while planning");
     }
+}
+
+}  // namespace
+
+namespace {
+
+ca_status_t set_kv_split_impl(ca_plan *p, int32_t visits_per_part) {
+    // everything is built and uploaded to a new list first; the plan changes
+    // only once that has succeeded
+    FwdList fwd;
+    build_fwd_items(p, visits_per_part, p->num_sms, &fwd);
+    if (static_cast<int64_t>(fwd.items.size()) > kI32Max)
+        return fail(CA_ERR_UNSUPPORTED, "the forward work list exceeds 2^31 items");
+    FwdItem *d_new = nullptr;
+    cudaError_t e = upload(&d_new, fwd.items, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();  // upload done; no launch still reads the old list
+    if (e != cudaSuccess) {
+        cudaFree(d_new);
+        return cuda_fail(e, "forward item upload");
+    }
+    cudaFree(p->d_fwd);
+    p->d_fwd = d_new;
+    p->kv_split = visits_per_part;
+    apply_fwd_counts(p, fwd);
+    set_workspace_bytes(p);
+    return CA_OK;
 }
 
 }  // namespace
@@ -410,23 +533,13 @@ ca_status_t build_host_plan_guarded(const ca_task_t *tasks, const ca_mask_t *mas
 // upload them; the workspace size may change.
 extern "C" ca_status_t ca_plan_set_kv_split(ca_plan_t *p, int32_t visits_per_part) {
     if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
-    std::vector<FwdItem> fwd;
-    const int32_t old = p->kv_split;
-    p->kv_split = visits_per_part;
-    build_fwd_items(p, &fwd);
-    set_workspace_bytes(p);
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) {
-        cudaFree(p->d_fwd);
-        p->d_fwd = nullptr;
-        e = upload(&p->d_fwd, fwd, nullptr);
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    const ca_status_t st = check_plan_device(p);
+    if (st != CA_OK) return st;
+    try {
+        return set_kv_split_impl(p, visits_per_part);
+    } catch (const std::bad_alloc &) {
+        return fail(CA_ERR_INVALID_ARG, "host memory exhausted while re-cutting the forward items");
     }
-    if (e != cudaSuccess) {
-        p->kv_split = old;
-        return cuda_fail(e, "forward item upload");
-    }
-    return CA_OK;
 }
 
 namespace {
@@ -453,7 +566,8 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
                                    const ca_shape_t *shape, ca_plan_info_t *info, int64_t *task_pairs) {
     if (!info) return fail(CA_ERR_INVALID_ARG, "info is NULL");
     HostPlan hp;
-    ca_status_t st = build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st = build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape,
+                                             kDryRunSms, &hp);
     if (st == CA_OK) {
         fill_info(hp.p, info);
         if (task_pairs) std::copy(hp.p->task_pairs.begin(), hp.p->task_pairs.end(), task_pairs);
@@ -479,27 +593,35 @@ ca_status_t ca_plan_create_masked(const ca_task_t *tasks, const ca_mask_t *masks
                                   const ca_shape_t *shape, void *upload_stream, ca_plan_t **out) {
     if (!out) return fail(CA_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
+    // The device's SM count sizes the forward split; argument errors are
+    // still reported before device errors.
+    int device = -1;
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDevice(&device);
+    const char *what = "cudaGetDevice";
+    if (e == cudaSuccess) {
+        e = cudaGetDeviceProperties(&prop, device);
+        what = "cudaGetDeviceProperties";
+    }
+    const int32_t num_sms = e == cudaSuccess ? prop.multiProcessorCount : kDryRunSms;
     HostPlan hp;
-    ca_status_t st = build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, &hp);
+    ca_status_t st =
+        build_host_plan_guarded(tasks, masks, n_tasks, doc_len, doc_kv_offset, n_docs, shape, num_sms, &hp);
     if (st != CA_OK) {
         delete hp.p;
         return st;
     }
     ca_plan *p = hp.p;
-    cudaError_t e = cudaGetDevice(&p->device);
-    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
-    cudaDeviceProp prop;
-    e = cudaGetDeviceProperties(&prop, p->device);
-    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDeviceProperties"); }
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, what); }
+    p->device = device;
     if (prop.major != 10 || prop.minor != 3) {
         delete p;
         return fail(CA_ERR_NO_DEVICE, "current device is sm_" + std::to_string(prop.major) +
                                           std::to_string(prop.minor) + ", the kernels are built for sm_103a");
     }
-    p->num_sms = prop.multiProcessorCount;
     cudaStream_t s = static_cast<cudaStream_t>(upload_stream);
     if ((e = upload(&p->d_tasks, p->h_tasks, s)) != cudaSuccess ||
-        (e = upload(&p->d_fwd, hp.fwd, s)) != cudaSuccess || (e = upload(&p->d_bwd, hp.bwd, s)) != cudaSuccess ||
+        (e = upload(&p->d_fwd, hp.fwd.items, s)) != cudaSuccess || (e = upload(&p->d_bwd, hp.bwd, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_task_ptr, hp.ptr, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_tasks, hp.dtasks, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_info, hp.doc_info, s)) != cudaSuccess ||
@@ -527,8 +649,13 @@ ca_status_t ca_plan_task_pairs(const ca_plan_t *p, int64_t *out) {
 
 void ca_plan_destroy(ca_plan_t *p) {
     if (!p) return;
+    // free on the plan's device, whichever device the caller has current
+    int cur = -1;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != p->device &&
+                          cudaSetDevice(p->device) == cudaSuccess;
     cudaDeviceSynchronize();
     free_device(p);
+    if (switched) cudaSetDevice(cur);
     delete p;
 }
 
@@ -554,8 +681,21 @@ ca_status_t ca_forward(const ca_plan_t *p, const void *q, const void *k, const v
     if (!q || !k || !v || !o || !lse || !workspace) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
         return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    if (o == q || o == k || o == v || static_cast<void *>(lse) == o)
-        return fail(CA_ERR_INVALID_ARG, "outputs alias inputs");
+    const BufferSizes b = buffer_sizes(p);
+    // outputs (o, lse, the workspace) must not share a byte with each other or with an input
+    const void *out[] = {o, lse, workspace};
+    const int64_t out_n[] = {b.o, b.lse, p->workspace_bytes};
+    const void *in[] = {q, k, v};
+    const int64_t in_n[] = {b.q, b.kv, b.kv};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = i + 1; j < 3; ++j)
+            if (overlap(out[i], out_n[i], out[j], out_n[j])) return fail(CA_ERR_INVALID_ARG, "output buffers overlap");
+        for (int j = 0; j < 3; ++j)
+            if (overlap(out[i], out_n[i], in[j], in_n[j]))
+                return fail(CA_ERR_INVALID_ARG, "an output buffer overlaps an input");
+    }
+    const ca_status_t st = check_plan_device(p);
+    if (st != CA_OK) return st;
     cudaError_t e = launch_forward(p, q, k, v, o, lse, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return CA_OK;
@@ -565,12 +705,10 @@ ca_status_t ca_backward(const ca_plan_t *p, const void *q, const void *k, const 
                         const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
                         void *stream) {
     if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
-    if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
-        return fail(CA_ERR_INVALID_ARG, "NULL pointer");
-    const void *ptrs[] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
-    for (const void *x : ptrs)
-        if (!aligned16(x)) return fail(CA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    if (dq == dk || dq == dv || dk == dv) return fail(CA_ERR_INVALID_ARG, "gradient outputs alias");
+    if (!workspace) return fail(CA_ERR_INVALID_ARG, "NULL pointer");
+    ca_status_t st = check_backward_args(p, q, k, v, o, lse, d_o, dq, dk, dv, workspace, p->workspace_bytes);
+    if (st != CA_OK) return st;
+    if ((st = check_plan_device(p)) != CA_OK) return st;
     cudaError_t e = launch_backward(p, q, k, v, o, lse, d_o, dq, dk, dv, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return CA_OK;
@@ -604,6 +742,8 @@ ca_status_t ca_merge(int32_t n_parts, const void *const *o_parts, const float *c
 
 ca_status_t ca_device_status(const ca_plan_t *p, void *stream) {
     if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    const ca_status_t st = check_plan_device(p);
+    if (st != CA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t word = 0;
     cudaError_t e = cudaMemcpyAsync(&word, p->d_err, sizeof(word), cudaMemcpyDeviceToHost, s);
@@ -619,6 +759,8 @@ ca_status_t ca_device_status(const ca_plan_t *p, void *stream) {
 
 ca_status_t ca_watchdog_selftest(const ca_plan_t *p, int64_t limit_ns, void *stream) {
     if (!p || limit_ns < 0) return fail(CA_ERR_INVALID_ARG, "bad plan or limit");
+    const ca_status_t st = check_plan_device(p);
+    if (st != CA_OK) return st;
     cudaError_t e = launch_watchdog_selftest(p, limit_ns, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "watchdog self-test launch");
     return CA_OK;

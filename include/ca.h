@@ -11,11 +11,17 @@
  * "Property 2: Composability").
  *
  * Every call takes plain device pointers owned by the caller.  Nothing here
- * allocates device memory except ca_plan_create (the plan's own metadata).
- * All argument errors are detected on the host before any launch and returned
- * as a status; the library never aborts the process.  Functions are safe to
- * call from several host threads on distinct plans; one plan may be used
- * concurrently on several streams if each call has its own workspace.
+ * allocates device memory except ca_plan_create (the plan's own metadata) and
+ * ca_plan_set_kv_split (the plan's re-cut forward list).  All argument errors
+ * are detected on the host before any launch and returned as a status; the
+ * library never aborts the process.  Functions are safe to call from several
+ * host threads on distinct plans; one plan may be used concurrently on
+ * several streams if each call has its own workspace.  Three calls change a
+ * plan -- ca_plan_set_kv_split, ca_plan_set_wait_limit and
+ * ca_plan_set_timing_events -- and must not race with any other call on the
+ * same plan from another host thread.  Every call that takes a plan needs
+ * the device the plan was created on to be current (CA_ERR_INVALID_ARG
+ * otherwise, before any launch).
  *
  * Layouts (all token-major, row-major, densely packed):
  *   q, o, dq, d_o : [total_q, num_q_heads, head_dim]   -- the query rows of
@@ -95,8 +101,10 @@ typedef struct {
 /*
  * Validate the tasks and documents and build the plan: per-task pair counts,
  * the forward tile list (fully masked key tiles never appear) and the
- * backward tile list, both in longest-first order, uploaded to the current
- * device on upload_stream (a cudaStream_t; NULL = default stream).  The
+ * backward tile list, both grouped per (document, kv head) with the groups
+ * of most work first and the longest items first inside a group, uploaded to
+ * the current device on upload_stream (a cudaStream_t; NULL = default
+ * stream).  The
  * upload is synchronised before return.  The host arrays are only read.
  * Errors: CA_ERR_INVALID_ARG for n_tasks < 1, n_docs < 1, q_len < 1,
  * kv_len < 1, q_start < 0, kv_start < 0, q_start + q_len > doc_len,
@@ -171,10 +179,13 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
  * decode and pass-Q shapes (few query rows, long contexts) and the tail of
  * very long rows.  visits_per_part > 0: that size; < 0: never split; 0
  * (the default of every plan): split only when the launch has fewer than 4
- * waves of items (608 on a 152-SM GPU), into parts of (total key-tile
- * visits / 152) clamped to [64, 128] tiles.  Rebuilds and
- * uploads the plan's forward list (synchronises the device first); the
- * workspace size in ca_plan_info may change.
+ * waves of items (4 x the device's SM count: 608 on a 152-SM GB300), into
+ * parts of (total key-tile visits / SM count) clamped to [64, 128] tiles.
+ * Builds and uploads a new forward list (a device allocation), synchronises
+ * the device so that no enqueued launch still reads the old list, then
+ * swaps it in; the workspace size in ca_plan_info may change.  On any error
+ * the plan is left as it was.  It changes the plan: no other host thread
+ * may use the plan meanwhile.
  */
 ca_status_t ca_plan_set_kv_split(ca_plan_t *plan, int32_t visits_per_part);
 
@@ -184,8 +195,8 @@ ca_status_t ca_plan_info(const ca_plan_t *plan, ca_plan_info_t *out);
 /* Causal pairs of every task (per head), out[n_tasks]. */
 ca_status_t ca_plan_task_pairs(const ca_plan_t *plan, int64_t *out);
 
-/* Free the plan and its device metadata (synchronises the device first).
- * NULL is ignored. */
+/* Free the plan and its device metadata (synchronises the plan's device
+ * first; the caller's current device is restored).  NULL is ignored. */
 void ca_plan_destroy(ca_plan_t *plan);
 
 /*
@@ -196,7 +207,10 @@ void ca_plan_destroy(ca_plan_t *plan);
  * workspace: ca_plan_info().workspace_bytes bytes of device memory (the
  * forward uses a work-queue counter in it).  Asynchronous on stream; launch
  * failures return CA_ERR_CUDA.  Device-side watchdog/bounds failures are
- * reported by ca_device_status.
+ * reported by ca_device_status.  CA_ERR_INVALID_ARG before any launch for
+ * NULL or unaligned pointers, an output (o, lse, workspace) that shares a
+ * byte with another output or with q, k or v (sizes from the plan), or a
+ * current device other than the plan's.
  */
 ca_status_t ca_forward(const ca_plan_t *plan, const void *q, const void *k, const void *v,
                        void *o, float *lse, void *workspace, void *stream);
@@ -212,7 +226,10 @@ ca_status_t ca_forward(const ca_plan_t *plan, const void *q, const void *k, cons
  * document (0 where no task sees the key); rows outside all documents are not
  * written.  o and lse are the forward's outputs (o in the plan's o_dtype).
  * workspace: ca_plan_info().workspace_bytes bytes (fp32 dQ accumulator and
- * the D vector).
+ * the D vector).  CA_ERR_INVALID_ARG before any launch for NULL or unaligned
+ * pointers, an output (dq, dk, dv, workspace) that shares a byte with another
+ * output or with an input (q, k, v, o, lse, d_o), or a current device other
+ * than the plan's.
  */
 ca_status_t ca_backward(const ca_plan_t *plan, const void *q, const void *k, const void *v,
                         const void *o, const float *lse, const void *d_o,
@@ -225,13 +242,18 @@ ca_status_t ca_backward(const ca_plan_t *plan, const void *q, const void *k, con
  * plug-in code handed only its input and output buffers.  The papers have no
  * counterpart to this entry point; it exists for such callers only.
  *
- * The scratch (fp32 dQ accumulator and D vector) lives in one file-scope
- * device array of 16 MiB that every GPU loading libca.so holds until the
- * process exits.  Plans whose ca_plan_info().workspace_bytes exceed 16 MiB
- * are rejected with CA_ERR_UNSUPPORTED before any launch.  The entry point
- * calls no cudaMalloc, cudaFree or other allocating routine.  The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
+ * The scratch (fp32 dQ accumulator, D vector and work-queue counters:
+ * total_q * num_q_heads * (head_dim + 1) * 4 bytes, each part rounded up to
+ * 256, plus 256) lives in one file-scope device array of 16 MiB that every
+ * GPU loading libca.so holds until the process exits.  Plans whose backward
+ * scratch exceeds 16 MiB are rejected with CA_ERR_UNSUPPORTED before any
+ * launch (the split-KV scratch of the forward, also counted in
+ * ca_plan_info().workspace_bytes, is not needed here).  The entry point calls
+ * no cudaMalloc, cudaFree or other allocating routine.  A call made outside a
+ * stream capture looks up the array's device address (cudaGetSymbolAddress)
+ * with the plan's device current; a call inside a capture reuses the address
+ * of the last call outside one, so make the first call on a device before
+ * any stream capture.
  * All calls on a device share the array: calls that overlap on the GPU (on
  * different streams, or from several threads) race and give wrong results,
  * so serialise them.  The array keeps the last call's contents; every call
@@ -268,7 +290,8 @@ ca_status_t ca_merge(int32_t n_parts, const void *const *o_parts, const float *c
 ca_status_t ca_device_status(const ca_plan_t *plan, void *stream);
 
 /* Set the bounded-wait limit (nanoseconds, default 2e9) of the plan's
- * kernels.  Used by tests to exercise the watchdog path. */
+ * kernels.  Used by tests to exercise the watchdog path.  It changes the
+ * plan: no other host thread may use the plan meanwhile. */
 ca_status_t ca_plan_set_wait_limit(ca_plan_t *plan, int64_t ns);
 
 /*
@@ -287,7 +310,8 @@ ca_status_t ca_watchdog_selftest(const ca_plan_t *plan, int64_t limit_ns, void *
  * after it, events[4] after the main kernel and events[5] after the dQ
  * finalize kernel, all on the call's stream.  events is a host array of
  * n_events (>= 6) cudaEvent_t handles owned by the caller; pass NULL to stop.
- * The plan keeps the pointer, not a copy of the array.
+ * The plan keeps the pointer, not a copy of the array.  It changes the plan:
+ * no other host thread may use the plan meanwhile.
  */
 ca_status_t ca_plan_set_timing_events(ca_plan_t *plan, void *const *events, int32_t n_events);
 
