@@ -10,12 +10,16 @@ The metric counts 12 * head_dim * H_q FLOPs per causal (token, key) pair:
 Printed (rank 0, one JSON line): whole-job TFLOP/s over the timed steps with
 inputs resident in HBM (`value`), the same through the C ABI with host
 buffers (`e2e`: pinned host -> device copies of Q, K, V, dO and device -> host
-copies of dQ, dK, dV of every step inside the timed region, the copies of the
-next and previous steps overlapping each step's compute on their own streams;
-the one-stream serial schedule is reported beside it), the roofline of the dominant
-kernel (the backward main kernel, timed live with CUDA events on its stream),
-the clocks seen during the timed region, and the fp64 oracle timed on the host
-cores on a bounded sample of the same workload (`cpu_baseline`).
+copies of O, LSE, dQ, dK, dV of every step inside the timed region, the copies
+of the next and previous steps overlapping each step's compute on their own
+streams; the one-stream serial schedule is reported beside it), the roofline
+of the dominant kernel (the backward main kernel, timed live with CUDA events
+on its stream), the clocks seen during the timed region, a sustained region of
+at least 2.5 s of back-to-back steps with its clock samples binned by SM MHz
+(`sustained`), the rebatched CA-task pool and the 512K long-context chunk
+timed per launch (`more_configs`), and the fp64 oracle timed on the host cores
+on a bounded sample of the same workload (`cpu_baseline`, with the full
+chunk's time extrapolated from it and labelled as such).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -105,14 +109,18 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None, bins=False):
+        """Median / min SM clock, max power and the throttle reasons seen in
+        [t0, t1] (default: the marked region); with bins, the sample count per
+        30 MHz bin of SM clock."""
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        rows = [r for t, r in self.rows
-                if self.t0 is None or self.t1 is None or self.t0 <= t <= self.t1 + 0.05]
+        t0 = self.t0 if t0 is None else t0
+        t1 = self.t1 if t1 is None else t1
+        rows = [r for t, r in self.rows if t0 is None or t1 is None or t0 <= t <= t1 + 0.05]
         if not rows:
             rows = [r for _, r in self.rows]
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
@@ -124,9 +132,16 @@ class ClockSampler:
             for n, v in zip(names, r[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "power_w_max": max(pw) if pw else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "power_w_max": max(pw) if pw else None,
+               "reasons": sorted(reasons), "samples": len(rows)}
+        if bins:
+            hist = {}
+            for x in sm:
+                b = int(x // 30 * 30)
+                hist[f"{b}-{b + 29}"] = hist.get(f"{b}-{b + 29}", 0) + 1
+            out["sm_mhz_bins"] = dict(sorted(hist.items()))
+        return out
 
 
 def measured_traffic(kernel_file="traffic_bwd_main_llama8b_chunk_64k.json"):
@@ -261,8 +276,8 @@ def run_reference(args, rank, world):
 
 def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_step):
     """The same step through the C ABI with host buffers: pinned host -> device
-    copies of Q, K, V, dO and device -> host copies of dQ, dK, dV inside the timed
-    region, every step.
+    copies of Q, K, V, dO and device -> host copies of O, LSE, dQ, dK, dV inside
+    the timed region, every step.
 
     Two schedules over the same host buffers.  Serial: one stream runs each
     step's copies in, forward, backward and copies out in turn.  Overlapped (the
@@ -280,20 +295,19 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
     hk = k.cpu().pin_memory()
     hv = v.cpu().pin_memory()
     hdo = do.cpu().pin_memory()
-    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
-    hdk = torch.empty(dk.shape, dtype=dk.dtype).pin_memory()
-    hdv = torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
-    h_in, h_out = (hq, hk, hv, hdo), (hdq, hdk, hdv)
+    h_out = tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, lse, dq, dk, dv))
+    h_in = (hq, hk, hv, hdo)
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = sum(x.numel() * x.element_size() for x in h_out)
     dev_in = [tuple(torch.empty_like(x) for x in (q, k, v, do)) for _ in range(2)]
-    dev_out = [tuple(torch.empty_like(x) for x in (dq, dk, dv)) for _ in range(2)]
+    # every slot has its own O and LSE: the forward's results leave the device too
+    dev_out = [tuple(torch.empty_like(x) for x in (o, lse, dq, dk, dv)) for _ in range(2)]
 
     def compute(slot):
         qi, ki, vi, doi = dev_in[slot]
-        dqo, dko, dvo = dev_out[slot]
-        plan.forward(qi, ki, vi, o, lse, ws, stream=sh)
-        plan.backward(qi, ki, vi, o, lse, doi, dqo, dko, dvo, ws, stream=sh)
+        oo, lo, dqo, dko, dvo = dev_out[slot]
+        plan.forward(qi, ki, vi, oo, lo, ws, stream=sh)
+        plan.backward(qi, ki, vi, oo, lo, doi, dqo, dko, dvo, ws, stream=sh)
 
     def serial_step():
         with torch.cuda.stream(stream):
@@ -356,6 +370,7 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
         raise RuntimeError("device error in the end-to-end region")
     return {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "copies": "in: Q, K, V, dO; out: O, LSE, dQ, dK, dV (pinned host buffers)",
             "schedule": "double-buffered: copies in of step k+1 and out of step k-1 on their own streams "
                         "during step k's compute",
             "serial_ms_per_step": serial_ms,
@@ -521,6 +536,66 @@ def measure_split_kv(args, dev, stream, pk):
     return out
 
 
+def measure_config(args, dev, stream, pk, name, steps):
+    """One more configuration of the same kernels, fwd+bwd: the rebatched
+    CA-task pool (131072 query tokens of token-granular shards of 16 documents
+    of 8K..128K tokens, 32 q / 8 kv heads) or the 512K long-context chunk (one
+    262144-token document plus lognormal documents, 64 q / 8 kv heads).  Per
+    launch CUDA events on the launching stream; TFLOP/s over counted causal
+    pairs (4 d forward, 8 d backward per pair per query head)."""
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    w = W.WORKLOADS[name](seed=args.seed)
+    q, k, v, do = W.make_tensors(w, device=dev)
+    plan = ca.Plan.from_workload(w, stream=stream)
+    info = plan.info()
+    ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    o, lse = ca.alloc_forward(plan, device=dev)
+    dq, dk, dv = ca.alloc_backward(plan, device=dev)
+    sh = stream.cuda_stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+
+    def step():
+        plan.forward(q, k, v, o, lse, ws, stream=sh)
+        plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws, stream=sh)
+
+    for _ in range(3):
+        step()
+    stream.synchronize()
+    t0 = time.time()
+    for s in range(steps):
+        plan.set_timing_events(ev[s])
+        step()
+    stream.synchronize()
+    t1 = time.time()
+    plan.set_timing_events(None)
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError(f"device error in the {name} measurement")
+    f_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    b_ms = float(np.mean([e[2].elapsed_time(e[5]) for e in ev]))
+    m_ms = float(np.mean([e[3].elapsed_time(e[4]) for e in ev]))
+    peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    ff, fb = info["flops_fwd"], info["flops_bwd"]
+    out = {"workload": w.name, "tokens": w.total_q, "documents": w.n_docs, "tasks": w.n_tasks,
+           "heads": f"{w.num_q_heads}q/{w.num_kv_heads}kv", "causal_pairs_per_head": info["causal_pairs"],
+           "steps": steps, "warmup": 3, "forward_ms": f_ms, "backward_ms": b_ms, "bwd_main_ms": m_ms,
+           "forward_tflops": ff / (f_ms * 1e-3) / 1e12, "backward_tflops": fb / (b_ms * 1e-3) / 1e12,
+           "fwd_bwd_tflops": (ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12,
+           "pct_of_burst_peak": 100.0 * (ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12 / peak,
+           "roofline": {"kernel": "ca_bwd_main_kernel", "bound": "tensor", "unit": "TFLOP/s", "peak": peak,
+                        "achieved": fb / (m_ms * 1e-3) / 1e12, "frac": fb / (m_ms * 1e-3) / 1e12 / peak},
+           "forward_roofline": {"kernel": "ca_fwd_kernel", "bound": "tensor", "unit": "TFLOP/s", "peak": peak,
+                                "achieved": ff / (f_ms * 1e-3) / 1e12, "frac": ff / (f_ms * 1e-3) / 1e12 / peak},
+           "window": (t0, t1)}
+    plan.close()
+    del q, k, v, do, o, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local):
@@ -579,11 +654,34 @@ def run_gpu(args, rank, world, local):
     plan.set_timing_events(None)
     torch.cuda.synchronize()
     barrier(world)
-    clocks.stop()
     if plan.device_status(stream=sh) != 0:
         raise RuntimeError("device error in the timed region")
     ms_local = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms_local, world)
+
+    # ---- a sustained region of at least 2 s of back-to-back steps (the clock
+    # under a long load settles below its burst value; samples binned by MHz)
+    sustained = None
+    if not args.no_sustained:
+        n_sus = max(args.steps, int(np.ceil(args.sustained_s * 1e3 / ms_local)))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        w0 = time.time()
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            for _ in range(n_sus):
+                step()
+            s1.record(stream)
+        stream.synchronize()
+        w1 = time.time()
+        barrier(world)
+        if plan.device_status(stream=sh) != 0:
+            raise RuntimeError("device error in the sustained region")
+        sus_ms = max_over_ranks(s0.elapsed_time(s1) / n_sus, world)
+        sustained = {"steps": n_sus, "seconds": sus_ms * n_sus * 1e-3, "ms_per_step": sus_ms,
+                     "value": flops_step * world / (sus_ms * 1e-3) / 1e12, "unit": UNIT,
+                     "window": (w0, w1)}
     value = flops_step * world / (ms * 1e-3) / 1e12
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     pre_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
@@ -605,9 +703,25 @@ def run_gpu(args, rank, world, local):
     decode = None
     if not args.no_decode:
         decode = measure_decode(args, dev, stream, pk)
+    more = {}
+    if not args.no_more_configs:
+        more["rebatched_pool"] = measure_config(args, dev, stream, pk, "pool", steps=8)
+        more["long_context_chunk"] = measure_config(args, dev, stream, pk, "long", steps=3)
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
     peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     main_tf = info["flops_bwd"] / (main_ms * 1e-3) / 1e12
+
+    clocks.stop()
+    if sustained is not None:
+        w0, w1 = sustained.pop("window")
+        sustained["clocks"] = clocks.summary(w0, w1, bins=True)
+        c = sustained["clocks"]
+        if c["sm_mhz"] and c["sm_max_mhz"]:
+            # time x median clock: what the same work takes at the maximum clock if it scales with the clock
+            sustained["ms_per_step_at_max_clock_est"] = sustained["ms_per_step"] * c["sm_mhz"] / c["sm_max_mhz"]
+    for name, m in more.items():
+        w0, w1 = m.pop("window")
+        m["clocks"] = clocks.summary(w0, w1)
 
     line = None
     if rank == 0:
@@ -623,6 +737,9 @@ def run_gpu(args, rank, world, local):
                               f"{int(oracle.task_pairs(wsamp).sum())} causal pairs/head) of the chunk, "
                               f"{wsamp.num_q_heads} query heads sharing {wsamp.num_kv_heads} KV head(s), full "
                               f"fp64 forward + backward; {t_cpu:.1f} s")}
+            cpu["extrapolated_full_s"] = flops_step / (cpu["value"] * 1e12)
+            cpu["extrapolation"] = ("extrapolation, not a measurement: the full chunk's counted FLOPs per step "
+                                    "divided by the sample's measured CPU rate")
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -657,6 +774,8 @@ def run_gpu(args, rank, world, local):
             "split_kv_prefill": split_kv,
             "sparse_masks": masks,
             "decode": decode,
+            "sustained": sustained,
+            "more_configs": more or None,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -679,6 +798,10 @@ def main():
     ap.add_argument("--no-split-kv", action="store_true", help="skip the split-KV prefill + merge measurement")
     ap.add_argument("--no-masks", action="store_true", help="skip the sparse-mask measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode (split-KV) measurement")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the sustained (>= 2 s) region")
+    ap.add_argument("--sustained-s", type=float, default=2.5, help="length of the sustained region (seconds)")
+    ap.add_argument("--no-more-configs", action="store_true",
+                    help="skip the rebatched-pool and 512K-chunk measurements")
     ap.add_argument("--tokens", type=int, default=65536,
                     help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.gpu
 def test_bench_line_has_the_contract_fields():
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--tokens", "16384", "--steps", "3", "--warmup", "3",
-           "--no-cpu-baseline", "--no-split-kv", "--no-masks", "--no-decode"]
+           "--no-cpu-baseline", "--no-split-kv", "--no-masks", "--no-decode", "--no-more-configs",
+           "--sustained-s", "0.5"]
     r = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
@@ -41,6 +42,11 @@ def test_bench_line_has_the_contract_fields():
     # overlapped schedule is no slower than the serial one beyond noise
     assert e2e["ms_per_step"] >= 0.9 * d["ms_per_step"]
     assert e2e["ms_per_step"] <= 1.1 * e2e["serial_ms_per_step"]
+    # out: O (bf16), LSE, dQ, dK, dV; in: Q, K, V, dO -- the outputs carry LSE on top
+    assert e2e["d2h_bytes_per_step"] == e2e["h2d_bytes_per_step"] + 16384 * 32 * 4
+    sus = d["sustained"]
+    assert sus["steps"] >= 3 and sus["value"] > 0 and sus["seconds"] >= 0.4
+    assert sum(sus["clocks"]["sm_mhz_bins"].values()) == sus["clocks"]["samples"]
     assert d["gpu_launches"] > 0
     assert d["clocks"]["samples"] >= 1 and d["clocks"]["sm_max_mhz"] > 0
     assert d["cpu_baseline"] is None  # skipped here by --no-cpu-baseline

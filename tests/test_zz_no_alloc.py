@@ -5,13 +5,16 @@ library's own 16 MiB device scratch array instead of a caller workspace.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.  It checks, through the C ABI, that two calls in
-a row give the results of ca_backward (with a caller workspace) within the
-gradient tolerance of the parity tests, and that a plan needing more scratch
-than the array holds is refused before any launch."""
+a row give the results of ca_backward (with a caller workspace) and of the fp64
+oracle within the gradient tolerance of the parity tests, that a decode-shaped
+plan whose workspace is large only because of the forward's split-KV scratch
+is accepted, and that a plan whose backward needs more scratch than the array
+holds is refused before any launch."""
 import pytest
 import torch
 
 import document_masked_core_gb300 as ca
+import oracle
 import workloads as W
 from cases import EDGE
 from parity import check_grad, to64
@@ -46,6 +49,35 @@ def test_noalloc_backward_matches_workspace_backward_twice():
         assert plan.device_status() == 0
         for name, x, r in zip(("dQ", "dK", "dV"), out, ref):
             check_grad(to64(x), to64(r), name)
+    # the last call's results against the fp64 oracle (independent of ca_backward)
+    dQ, dK, dV = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    inside = torch.zeros(w.total_kv, dtype=torch.bool)
+    for off, L in zip(w.doc_kv_offset, w.doc_len):
+        inside[int(off):int(off + L)] = True
+    check_grad(to64(out[0]), dQ, "dQ vs oracle")
+    check_grad(to64(out[1])[inside.numpy()], dK[inside.numpy()], "dK vs oracle")
+    check_grad(to64(out[2])[inside.numpy()], dV[inside.numpy()], "dV vs oracle")
+
+
+def test_noalloc_accepts_decode_plan_with_large_forward_scratch():
+    """Four decode rows against 32K cached tokens: the forward's split-KV
+    partials make the workspace larger than 16 MiB, while the backward needs
+    only 66 KB of it."""
+    w = W.decode_batch(n_seq=4, context=32768)
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    plan = ca.Plan.from_workload(w)
+    assert plan.info()["workspace_bytes"] > 16 << 20
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    ref = ca.alloc_backward(plan)
+    plan.backward(q, k, v, o, lse, do, *ref, ws)
+    out = ca.alloc_backward(plan)
+    plan.backward_noalloc(q, k, v, o, lse, do, *out)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    for name, x, r in zip(("dQ", "dK", "dV"), out, ref):
+        check_grad(to64(x), to64(r), name)
 
 
 def test_noalloc_rejects_plans_beyond_the_scratch():
