@@ -557,6 +557,9 @@ def measure_config(args, dev, stream, pk, name, steps):
     dq, dk, dv = ca.alloc_backward(plan, device=dev)
     sh = stream.cuda_stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for row in ev:  # torch creates the underlying cudaEvent on first record
+        for e in row:
+            e.record(stream)
 
     def step():
         plan.forward(q, k, v, o, lse, ws, stream=sh)

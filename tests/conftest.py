@@ -24,3 +24,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With CA_PARITY_REPORT=<path>, write the largest parity error per test
+    and quantity (tests/parity.py) as JSON."""
+    path = os.environ.get("CA_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    try:
+        import parity
+    except ImportError:
+        return
+    with open(path, "w") as f:
+        json.dump(parity.REPORT, f, indent=1, sort_keys=True)
