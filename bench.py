@@ -145,9 +145,10 @@ class ClockSampler:
 
 
 def measured_traffic(kernel_file="traffic_bwd_main_llama8b_chunk_64k.json"):
-    """DRAM bytes per launch of the backward main kernel from the committed
-    ncu summary, or None when the kernel's sources have changed since the
-    capture (their hash differs) or no summary exists."""
+    """DRAM bytes per launch of one kernel from its committed ncu summary
+    (default: the backward main kernel), or None when the kernel's sources
+    have changed since the capture (their hash differs) or no summary
+    exists."""
     import hashlib
     path = os.path.join(ROOT, "profiles", kernel_file)
     try:
@@ -773,6 +774,13 @@ def run_gpu(args, rank, world, local):
                          "traffic_unit": "bytes per launch (ncu dram read + write, profiles/)",
                          "peak_kind": f"bf16 burst, {pk_kind}",
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
+            "forward_roofline": {"kernel": "ca_fwd_kernel", "bound": "tensor",
+                                 "achieved": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12, "peak": peak,
+                                 "unit": "TFLOP/s", "frac": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12 / peak,
+                                 "traffic": measured_traffic("traffic_fwd_llama8b_chunk_64k.json"),
+                                 "traffic_unit": "bytes per launch (ncu dram read + write, profiles/)",
+                                 "algorithmic": "4*head_dim*H_q*causal_pairs per launch; algorithmic bytes "
+                                                "Q, K, V, O, LSE once = 1.30 GB"},
             "e2e": e2e,
             "split_kv_prefill": split_kv,
             "sparse_masks": masks,
