@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(320, 1)
             bool ok = true;
             for (uint32_t r = 0; ok; ++r) {
                 // take the next item and publish it to the other roles
-                if (!(ok = mbar_wait(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1, wd))) break;
+                if (!(ok = mbar_wait_ool(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1, wd))) break;
                 int32_t idx = atomicAdd(p.sched, 1);
                 if (idx >= p.n_items) idx = -1;
                 bars.ring[r & 3] = idx;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     if (gi.t[x].n_kv == 0) continue;
-                    if (!(ok = mbar_wait(&bars.q_empty[x], (q_it[x] & 1) ^ 1, wd))) break;
+                    if (!(ok = mbar_wait_ool(&bars.q_empty[x], (q_it[x] & 1) ^ 1, wd))) break;
                     mbar_arrive_expect_tx(&bars.q_full[x], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
@@ -324,14 +324,14 @@ __global__ void __launch_bounds__(320, 1)
                     // K and V stages are released separately: K once both query tiles'
                     // S products have read it (an iteration before V), so each K load has
                     // about two iterations to land before its S product
-                    if (!(ok = mbar_wait(&bars.k_empty[st], ph ^ 1, wd))) break;
+                    if (!(ok = mbar_wait_ool(&bars.k_empty[st], ph ^ 1, wd))) break;
                     const int32_t key_row = gi.kv_off + gi.kr.tile(gi.i0 + i) * kTileKeys;
                     mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
                         tma_load_3d(sK + st * C::kTileBytes + h * C::kHalfBytes, &tm_k, &bars.k_full[st], h * 64,
                                     gi.g, key_row);
-                    if (!(ok = mbar_wait(&bars.v_empty[st], ph ^ 1, wd))) break;
+                    if (!(ok = mbar_wait_ool(&bars.v_empty[st], ph ^ 1, wd))) break;
                     mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(320, 1)
             // released after tile B's, or after A's when B does not visit it
             auto issue_s = [&](int x, uint32_t kvi, int32_t i) -> bool {
                 const uint32_t st = kvi % C::kStages;
-                if (!mbar_wait(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
+                if (!mbar_wait_ool(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
                 tc_fence_after();
                 const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
                 const uint32_t bd = sdesc_lo(k_base + st * C::kTileBytes, 16);
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(320, 1)
                 return true;
             };
             for (uint32_t r = 0; ok; ++r) {
-                if (!(ok = mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
+                if (!(ok = mbar_wait_ool(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
                 const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
                 mbar_arrive(&bars.ring_empty[r & 3]);
                 if (idx < 0) break;
@@ -380,19 +380,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     if (nk[x] == 0) continue;
-                    if (!(ok = mbar_wait(&bars.q_full[x], q_it[x] & 1, wd))) break;
+                    if (!(ok = mbar_wait_ool(&bars.q_full[x], q_it[x] & 1, wd))) break;
                     tc_fence_after();
                     if (!(ok = issue_s(x, kv_it, 0))) break;
                 }
                 for (int32_t i = 0; i < gi.n_kv && ok; ++i) {
                     const uint32_t kvi = kv_it + i;
                     const uint32_t st = kvi % C::kStages;
-                    if (!(ok = mbar_wait(&bars.v_full[st], (kvi / C::kStages) & 1, wd))) break;
+                    if (!(ok = mbar_wait_ool(&bars.v_full[st], (kvi / C::kStages) & 1, wd))) break;
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (i >= nk[x]) continue;
-                        if (!(ok = mbar_wait(&bars.p_full[x], s_it[x] & 1, wd))) break;
-                        if (i == 0 && !(ok = mbar_wait(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
+                        if (!(ok = mbar_wait_ool(&bars.p_full[x], s_it[x] & 1, wd))) break;
+                        if (i == 0 && !(ok = mbar_wait_ool(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
                         tc_fence_after();
                         const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                         const uint32_t d_o = tmem + C::kColO + x * D, a_p = tmem + C::kColS + x * 128;
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(320, 1)
             const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
             uint32_t zero = 0;
             const Watchdog wd2{&drain, &zero};
-            mbar_wait(&bars.mma_done, 0, wd2);
+            mbar_wait_ool(&bars.mma_done, 0, wd2);
         }
         __syncwarp();
     } else {
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t s_it = 0, o_it = 0;
         bool ok = true;
         for (uint32_t r = 0; ok; ++r) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
+            ok = __all_sync(0xffffffffu, mbar_wait_ool(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
             if (!ok) break;
             const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
             __syncwarp();
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             float m = -INFINITY, l = 0.f;
             for (int32_t i = 0; i < tg.n_kv; ++i, ++s_it) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[x], s_it & 1, wd));
+                ok = __all_sync(0xffffffffu, mbar_wait_ool(&bars.s_full[x], s_it & 1, wd));
                 if (!ok) break;
                 tc_fence_after();
                 // s_full also implies that PV_x(i-1) has completed (issued before S_x(i))
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             if (!ok) break;
             // epilogue: O / l and LSE once the last PV of this tile has landed
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_full[x], o_it & 1, wd));
+            ok = __all_sync(0xffffffffu, mbar_wait_ool(&bars.o_full[x], o_it & 1, wd));
             if (!ok) break;
             ++o_it;
             tc_fence_after();

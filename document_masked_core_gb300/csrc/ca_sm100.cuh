@@ -102,6 +102,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
+// The same bounded wait with its slow path out of line (static, one copy per
+// translation unit): every wait site is one poll and a call.  Shorter code
+// for roles whose register budget can take the call; measured faster in the
+// forward (2.952 against 3.035 ms on the 64K chunk) and slower in the
+// backward, whose MMA thread then saves and restores registers around the
+// call on its hand-offs (9.29 against 8.84 ms).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, const DevCtl *ctl,
+                                                   volatile uint32_t *abort_flag) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > ctl->wait_limit_ns) {
+            *abort_flag = 1u;
+            atomicOr(ctl->err, kErrTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait_ool(uint64_t *bar, uint32_t parity, const Watchdog &wd) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, wd.ctl, wd.abort_flag);
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
