@@ -84,3 +84,39 @@ def test_backward_is_deterministic_for_dk_dv():
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
     # dQ sums fp32 atomics in arbitrary order: equal to rounding
     assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2
+
+
+def test_overlapping_buffers_are_refused_before_any_launch():
+    """Outputs that share a byte with another output or with an input are
+    rejected with CA_ERR_INVALID_ARG (sizes from the plan), on the host."""
+    w = EDGE[0]
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    plan = ca.Plan.from_workload(w)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    dq, dk, dv = ca.alloc_backward(plan)
+    big = torch.empty(q.numel() * 4 + 4096, dtype=torch.uint8, device="cuda")
+
+    def refused(fn):
+        with pytest.raises(ca.CAError) as ei:
+            fn()
+        assert ei.value.status == ca.capi.CA_ERR_INVALID_ARG
+    # forward: O overlapping Q (offset by one 16-byte row chunk), LSE inside O, workspace over V
+    q_in_big = big[:q.numel() * 2].view(torch.bfloat16).view_as(q).copy_(q)
+    o_shift = big[16:16 + o.numel() * 2].view(torch.bfloat16).view_as(o)
+    refused(lambda: plan.forward(q_in_big, k, v, o_shift, lse, ws))
+    refused(lambda: plan.forward(q, k, v, o, o.view(torch.float32).view(-1)[:lse.numel()].view_as(lse), ws))
+    refused(lambda: plan.forward(q, k, v, o, lse, v.view(torch.uint8)))
+    plan.forward(q, k, v, o, lse, ws)
+    # backward: dK over V, dQ over the workspace, dV over dK
+    refused(lambda: plan.backward(q, k, v, o, lse, do, dq, v, dv, ws))
+    refused(lambda: plan.backward(q, k, v, o, lse, do, ws.view(torch.bfloat16)[:dq.numel()].view_as(dq), dk, dv, ws))
+    refused(lambda: plan.backward(q, k, v, o, lse, do, dq, dk, dk, ws))
+    # the refused calls launched nothing: a real backward still matches the first one
+    plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    ref = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    inside = doc_rows(w)
+    check_grad(to64(dq), ref[0], "dQ")
+    check_grad(to64(dk)[inside], ref[1][inside], "dK")
