@@ -20,6 +20,8 @@ Long-context Language Model Training by Core Attention Disaggregation, §3.4
 the summed dK/dV (dO zero on rows outside the pool) within the gradient
 tolerance.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -203,3 +205,25 @@ def test_masked_chunk_every_row_and_column(name):
         what = f"{name} doc {doc} (len {int(w.doc_len[doc])}) kv head {g}"
         check_doc(w, res, gpu, doc, g, what)
         check_cols(w, res, gpu, doc, g, np.arange(int(w.doc_len[doc])), what)
+
+
+@pytest.mark.skipif(os.environ.get("CA_LONG_PARITY") != "1",
+                    reason="about 10 minutes of oracle time: run with CA_LONG_PARITY=1")
+def test_long_chunk_early_columns_of_262k_document():
+    """The 262K document's earliest key columns (each depends on every later
+    row, 262K rows seeing up to 262K keys, one kv head) and stratified
+    columns across the document, element-wise against the oracle."""
+    w = W.long_context_chunk()
+    inputs = W.make_tensors(w, device="cuda")
+    gpu = gpu_run(w, inputs)
+    q, k, v, do = host_inputs(inputs)
+    doc = int(np.argmax(w.doc_len))
+    L = int(w.doc_len[doc])
+    g = 5
+    rng = np.random.default_rng(w.seed + 3000)
+    cols = np.unique(np.concatenate([np.arange(0, 128), np.arange(128, L, 4096), rng.integers(0, L, 256)]))
+    res = dense.document_group(w, q, k, v, do, doc, g, columns=cols)
+    what = f"long chunk doc {doc} (len {L}) kv head {g}, {len(cols)} columns from 0"
+    check_doc(w, res, gpu, doc, g, what)
+    e_k, e_v = check_cols(w, res, gpu, doc, g, cols, what)
+    print(f"{what}: dK {e_k:.2e}, dV {e_v:.2e}")
