@@ -208,7 +208,7 @@ def test_masked_chunk_every_row_and_column(name):
 
 
 @pytest.mark.skipif(os.environ.get("CA_LONG_PARITY") != "1",
-                    reason="about 10 minutes of oracle time: run with CA_LONG_PARITY=1")
+                    reason="about 23 minutes of oracle time on 16 host cores: run with CA_LONG_PARITY=1")
 def test_long_chunk_early_columns_of_262k_document():
     """The 262K document's earliest key columns (each depends on every later
     row, 262K rows seeing up to 262K keys, one kv head) and stratified
