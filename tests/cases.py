@@ -19,6 +19,11 @@ EDGE = [
                      hq=4, hkv=2, d=64),
     # split KV: four blocks of one document (pass-KV partials)
     W.split_kv_prefill(seed=5, n_new=96, cached=416, n_blocks=4, hq=8, hkv=1, d=128),
+    # G = 32, 64, 128: 4, 2 and 1 tokens per 128-row query tile; shards and ragged ends
+    W.custom("g32_d128_shards", [77, 300], [(1, 0, 150, 0, 150), (0, 0, 77, 0, 77), (1, 150, 150, 0, 300)],
+             hq=32, hkv=1, d=128, seed=6),
+    W.custom("g64_d64_blocks", [150], [(0, 0, 150, 0, 150), (0, 100, 50, 30, 100)], hq=64, hkv=1, d=64, seed=7),
+    W.custom("g128_d128", [40, 129], [(0, 0, 40, 0, 40), (1, 0, 129, 0, 129)], hq=128, hkv=1, d=128, seed=8),
 ]
 
 
