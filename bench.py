@@ -604,6 +604,64 @@ def measure_config(args, dev, stream, pk, name, steps):
     return out
 
 
+def measure_tiny(args, dev, stream):
+    """The tiny packed chunk (2048 tokens, documents of 1024, 512, 256 and 256
+    tokens, 4 q / 1 kv head, head_dim 64), which is launch-latency bound:
+    fwd+bwd per step issued call by call against the same two calls captured
+    once into a CUDA graph and replayed (both timed over back-to-back steps
+    with CUDA events)."""
+    import torch
+
+    import document_masked_core_gb300 as ca
+    import workloads as W
+
+    w = W.tiny_chunk(seed=args.seed)
+    q, k, v, do = W.make_tensors(w, device=dev)
+    plan = ca.Plan.from_workload(w, stream=stream)
+    info = plan.info()
+    ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    o, lse = ca.alloc_forward(plan, device=dev)
+    dq, dk, dv = ca.alloc_backward(plan, device=dev)
+    sh = stream.cuda_stream
+
+    def step():
+        plan.forward(q, k, v, o, lse, ws, stream=sh)
+        plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws, stream=sh)
+
+    n = 200
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        plan.forward(q, k, v, o, lse, ws)
+        plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    graph_ms = e0.elapsed_time(e1) / n
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the tiny-chunk measurement")
+    fl = info["flops_fwd"] + info["flops_bwd"]
+    out = {"workload": w.name, "steps": n, "eager_ms": eager_ms, "graph_ms": graph_ms,
+           "eager_tflops": fl / (eager_ms * 1e-3) / 1e12, "graph_tflops": fl / (graph_ms * 1e-3) / 1e12,
+           "bound": "launch latency (4 kernels and a memset per step)"}
+    plan.close()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local):
@@ -713,6 +771,7 @@ def run_gpu(args, rank, world, local):
         decode = measure_decode(args, dev, stream, pk)
     more = {}
     if not args.no_more_configs:
+        more["tiny_chunk"] = measure_tiny(args, dev, stream)
         more["rebatched_pool"] = measure_config(args, dev, stream, pk, "pool", steps=8)
         more["long_context_chunk"] = measure_config(args, dev, stream, pk, "long", steps=3)
     peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
@@ -728,8 +787,9 @@ def run_gpu(args, rank, world, local):
             # time x median clock: what the same work takes at the maximum clock if it scales with the clock
             sustained["ms_per_step_at_max_clock_est"] = sustained["ms_per_step"] * c["sm_mhz"] / c["sm_max_mhz"]
     for name, m in more.items():
-        w0, w1 = m.pop("window")
-        m["clocks"] = clocks.summary(w0, w1)
+        if "window" in m:
+            w0, w1 = m.pop("window")
+            m["clocks"] = clocks.summary(w0, w1)
 
     line = None
     if rank == 0:

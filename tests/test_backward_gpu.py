@@ -120,3 +120,38 @@ def test_overlapping_buffers_are_refused_before_any_launch():
     inside = doc_rows(w)
     check_grad(to64(dq), ref[0], "dQ")
     check_grad(to64(dk)[inside], ref[1][inside], "dK")
+
+
+def test_forward_backward_replay_from_a_cuda_graph():
+    """ca_forward + ca_backward captured into a CUDA graph (stream capture; the
+    calls allocate nothing and every counter they use is reset on the device
+    each call) replay with the eager results: O, LSE, dK, dV bit for bit, dQ
+    (fp32 reduce-adds in any order) within the gradient tolerance of the
+    oracle, twice in a row."""
+    w = W.tiny_chunk()
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    plan = ca.Plan.from_workload(w)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    dq, dk, dv = ca.alloc_backward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    o2, lse2 = ca.alloc_forward(plan)
+    dq2, dk2, dv2 = ca.alloc_backward(plan)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.forward(q, k, v, o2, lse2, ws)
+        plan.backward(q, k, v, o2, lse2, do, dq2, dk2, dv2, ws)
+    ref = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    for _ in range(2):
+        for t in (o2, dq2, dk2, dv2):
+            t.fill_(float("nan"))
+        lse2.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert torch.equal(o2.view(torch.int16), o.view(torch.int16)) and torch.equal(lse2, lse)
+        assert torch.equal(dk2.view(torch.int16), dk.view(torch.int16))
+        assert torch.equal(dv2.view(torch.int16), dv.view(torch.int16))
+        check_grad(to64(dq2), ref[0], "dQ (graph replay)")
