@@ -26,7 +26,16 @@
 //
 // Warp roles (320 threads): warps 0-3 softmax + epilogue of tile A, warps 4-7
 // of tile B (thread i of a warpgroup <-> TMEM lane i <-> tile row i), warp 8
-// TMA producer, warp 9 TMEM owner + MMA issuer.
+// TMA producer, warp 9 TMEM owner + MMA issuer.  The producer and MMA warps
+// run their loops with all 32 lanes (every wait, count and descriptor is the
+// same in each lane) and one elected lane issues each copy or tcgen05 op: the
+// MMA warp's instruction stream is what paces the tensor core here, and with
+// a single lane issuing inside a lane-0 branch the forward ran 10-15 % slower.
+//
+// Across items the MMA warp keeps the tensor core fed: Q tiles go through a
+// three-slot ring, each slot released after its tile's last S product, and in
+// an item's last visit the next item's first S products take the places of
+// the missing S(j+1) products when their Q and K tiles have landed.
 #include <algorithm>
 #include <cmath>
 
@@ -55,14 +64,20 @@ struct FwdParams {
 template <int D>
 struct FwdCfg {
     static constexpr int kStages = 2;
+    // Q tiles go through a ring of three slots in the order they are loaded
+    // (an item's tile A, then its tile B): the next item's first tile loads
+    // into the free slot while the current item runs.
+    static constexpr int kQSlots = 3;
     static constexpr int kHalfBytes = 128 * 128;              // 128 rows x 64 bf16
     static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // 128 rows x D bf16
-    static constexpr int kOffQ = 0;                           // Q_A, Q_B
-    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQSlots * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
     static constexpr int kBarBytes = 512;  // FwdBars (checked below)
-    static constexpr int kSmemRaw = kOffBar + kBarBytes;
+    static constexpr int kOffRec = kOffBar + kBarBytes;
+    static constexpr int kRecBytes = 4 * 128;  // ItemRec ring (checked below)
+    static constexpr int kSmemRaw = kOffRec + kRecBytes;
     static constexpr int kSmemBytes = kSmemRaw > 122880 ? kSmemRaw : 122880;  // one CTA per SM
     static_assert(kSmemBytes <= 232448, "forward tiles exceed 227 KB of shared memory");
     static constexpr uint32_t kTmemCols = 512;
@@ -80,8 +95,7 @@ constexpr uint32_t kRingConsumers = 9;
 
 struct FwdBars {
     uint64_t ring_full[4], ring_empty[4];
-    int32_t ring[4];
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[3], q_empty[3];  // Q slot s (q_empty: committed after the tile's last S product)
     uint64_t k_full[2], v_full[2];
     uint64_t k_empty[2];  // committed after the last S product that reads the K tile
     uint64_t v_empty[2];  // committed after the last PV product that reads the V tile
@@ -144,6 +158,16 @@ __device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) 
     gi.n_kv = max(gi.t[0].n_kv, gi.t[1].n_kv);
     return gi;
 }
+
+// A work-queue entry as the producer publishes it: the item's index (-1 once
+// the queue is exhausted) and its decoded geometry, so the other roles read it
+// from shared memory instead of chasing the item and task tables in global
+// memory at each item start.
+struct ItemRec {
+    ItemGeo gi;
+    int32_t idx;
+};
+static_assert(sizeof(ItemRec) <= 128, "work-queue record exceeds its shared-memory slot");
 
 // Make the compiler treat the 32 registers as produced after the preceding
 // tcgen05.wait::ld (their values are only valid after it).
@@ -250,14 +274,17 @@ __global__ void __launch_bounds__(320, 1)
     uint8_t *sK = smem + C::kOffK;
     uint8_t *sV = smem + C::kOffV;
     FwdBars &bars = *reinterpret_cast<FwdBars *>(smem + C::kOffBar);
+    ItemRec *recs = reinterpret_cast<ItemRec *>(smem + C::kOffRec);  // [4], one per ring entry
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
 
     if (threadIdx.x == 0) {
+        for (int sl = 0; sl < C::kQSlots; ++sl) {
+            mbar_init(&bars.q_full[sl], 1);
+            mbar_init(&bars.q_empty[sl], 1);
+        }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(&bars.q_full[x], 1);
-            mbar_init(&bars.q_empty[x], 1);
             mbar_init(&bars.s_full[x], 1);
             mbar_init(&bars.p_full[x], 4);  // one arrival per warp
             mbar_init(&bars.o_full[x], 1);
@@ -294,128 +321,216 @@ __global__ void __launch_bounds__(320, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t kv_it = 0, q_it[2] = {0, 0};
+        // The producer publishes the work queue one item ahead of its own loads
+        // (each ring entry carries the decoded item), then loads the item's Q
+        // tiles into the Q slot ring and its K/V tiles into the two stages, in
+        // the order the MMA warp consumes them: Q_A, K(0), Q_B, V(0), K(1), V(1), ...
+        {
+            // the whole warp runs the loop; one elected lane issues each copy
+            auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait_ool(bar, parity, wd));
+            };
+            uint32_t kv_it = 0, qi = 0;
             bool ok = true;
-            for (uint32_t r = 0; ok; ++r) {
-                // take the next item and publish it to the other roles
-                if (!(ok = mbar_wait_ool(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1, wd))) break;
-                int32_t idx = atomicAdd(p.sched, 1);
+            auto publish = [&](uint32_t r, ItemGeo &gi) -> int32_t {
+                if (!(ok = wwait(&bars.ring_empty[r & 3], ((r >> 2) & 1) ^ 1))) return -1;
+                int32_t idx = 0;
+                if (lane == 0) idx = atomicAdd(p.sched, 1);
+                idx = __shfl_sync(0xffffffffu, idx, 0);
                 if (idx >= p.n_items) idx = -1;
-                bars.ring[r & 3] = idx;
-                mbar_arrive(&bars.ring_full[r & 3]);
-                if (idx < 0) break;
-                const ItemGeo gi = decode_item(p, idx);
-                if (gi.n_kv == 0) continue;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (gi.t[x].n_kv == 0) continue;
-                    if (!(ok = mbar_wait_ool(&bars.q_empty[x], (q_it[x] & 1) ^ 1, wd))) break;
-                    mbar_arrive_expect_tx(&bars.q_full[x], C::kTileBytes);
-#pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        tma_load_3d(sQ + x * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[x], h * 64,
-                                    gi.g * p.G, gi.t[x].row0);
-                    ++q_it[x];
+                if (idx >= 0) gi = decode_item(p, idx);
+                if (lane == 0) {
+                    if (idx >= 0) recs[r & 3].gi = gi;
+                    recs[r & 3].idx = idx;
+                    mbar_arrive(&bars.ring_full[r & 3]);  // release: the record is complete
                 }
-                for (int32_t i = 0; i < gi.n_kv && ok; ++i, ++kv_it) {
-                    const uint32_t st = kv_it % C::kStages;
-                    const uint32_t ph = (kv_it / C::kStages) & 1;
-                    // K and V stages are released separately: K once both query tiles'
-                    // S products have read it (an iteration before V), so each K load has
-                    // about two iterations to land before its S product
-                    if (!(ok = mbar_wait_ool(&bars.k_empty[st], ph ^ 1, wd))) break;
-                    const int32_t key_row = gi.kv_off + gi.kr.tile(gi.i0 + i) * kTileKeys;
-                    mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
+                __syncwarp();
+                return idx;
+            };
+            auto load_q = [&](const ItemGeo &gi, int x) -> bool {
+                const uint32_t sl = qi % C::kQSlots;
+                if (!wwait(&bars.q_empty[sl], ((qi / C::kQSlots) & 1) ^ 1)) return false;
+                mbar_arrive_expect_tx_w(&bars.q_full[sl], C::kTileBytes);
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        tma_load_3d(sK + st * C::kTileBytes + h * C::kHalfBytes, &tm_k, &bars.k_full[st], h * 64,
-                                    gi.g, key_row);
-                    if (!(ok = mbar_wait_ool(&bars.v_empty[st], ph ^ 1, wd))) break;
-                    mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d_w(sQ + sl * C::kTileBytes + h * C::kHalfBytes, &tm_q, &bars.q_full[sl], h * 64,
+                                gi.g * p.G, gi.t[x].row0);
+                ++qi;
+                return true;
+            };
+            // K and V stages are released separately: K once both query tiles' S
+            // products have read it (an iteration before V), so each K load has
+            // about two iterations to land before its S product
+            auto load_kv = [&](const ItemGeo &gi, int32_t i, bool v) -> bool {
+                const uint32_t kvi = kv_it + i;
+                const uint32_t st = kvi % C::kStages, ph = (kvi / C::kStages) & 1;
+                if (!wwait(v ? &bars.v_empty[st] : &bars.k_empty[st], ph ^ 1)) return false;
+                uint64_t *full = v ? &bars.v_full[st] : &bars.k_full[st];
+                const int32_t key_row = gi.kv_off + gi.kr.tile(gi.i0 + i) * kTileKeys;
+                mbar_arrive_expect_tx_w(full, C::kTileBytes);
+                uint8_t *dst = (v ? sV : sK) + st * C::kTileBytes;
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        tma_load_3d(sV + st * C::kTileBytes + h * C::kHalfBytes, &tm_v, &bars.v_full[st], h * 64,
-                                    gi.g, key_row);
-                }
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_3d_w(dst + h * C::kHalfBytes, v ? &tm_v : &tm_k, full, h * 64, gi.g, key_row);
+                return true;
+            };
+            // The next entry is published after the current item's first loads are
+            // in flight, so its decode (dependent global loads) overlaps them.
+            ItemGeo gi;
+            int32_t idx = publish(0, gi);
+            for (uint32_t r = 0; ok && idx >= 0; ++r) {
+                if (gi.n_kv > 0)
+                    ok = (gi.t[0].n_kv == 0 || load_q(gi, 0)) && load_kv(gi, 0, false) &&
+                         (gi.t[1].n_kv == 0 || load_q(gi, 1)) && load_kv(gi, 0, true);
+                if (!ok) break;
+                ItemGeo nx;
+                const int32_t nidx = publish(r + 1, nx);
+                if (!ok) break;
+                for (int32_t i = 1; i < gi.n_kv && ok; ++i) ok = load_kv(gi, i, false) && load_kv(gi, i, true);
+                kv_it += gi.n_kv;
+                gi = nx;
+                idx = nidx;
             }
-            if (!ok) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
+            if (!ok && lane == 0) __nanosleep(1000000);  // let copies already in flight land before the CTA drains
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0;
-            uint32_t s_it[2] = {0, 0}, q_it[2] = {0, 0}, o_it[2] = {0, 0};
+        // Per visit i of an item: PV_A(i), S_A(i+1), PV_B(i), S_B(i+1).  In an
+        // item's last visit, when both tiles end there, the next item's S_A(0)
+        // and S_B(0) take the places of the missing S(i+1) products, so the
+        // tensor core does not idle across the item boundary.
+        {
+            // the whole warp runs the loop; one elected lane issues each tcgen05 op
+            auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait_ool(bar, parity, wd));
+            };
+            uint32_t kv_it = 0, qi = 0, r = 0;
+            uint32_t s_it[2] = {0, 0}, o_it[2] = {0, 0};
             bool ok = true;
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-            int32_t nk1 = 0;  // key tiles tile B of the current item visits
-            // S_x = Q_x K^T into tile x's S columns, for the key tile of ring index kvi
-            // (entry i of the item); tile A's product comes first, so the K tile is
-            // released after tile B's, or after A's when B does not visit it
-            auto issue_s = [&](int x, uint32_t kvi, int32_t i) -> bool {
+            // S_x = Q K^T of the tile in Q ring slot q and the key tile of K ring index
+            // kvi, into tile x's S columns.  The K stage is released after the last S
+            // product that reads it (release_k: tile B's, or tile A's when B does not
+            // visit that key tile), the Q slot after its tile's last S product.
+            auto issue_s = [&](int x, uint32_t q, uint32_t kvi, bool release_k, bool release_q) -> bool {
                 const uint32_t st = kvi % C::kStages;
-                if (!mbar_wait_ool(&bars.k_full[st], (kvi / C::kStages) & 1, wd)) return false;
+                if (!wwait(&bars.k_full[st], (kvi / C::kStages) & 1)) return false;
                 tc_fence_after();
-                const uint32_t ad = sdesc_lo(q_base + x * C::kTileBytes, 16);
+                const uint32_t ad = sdesc_lo(q_base + (q % C::kQSlots) * C::kTileBytes, 16);
                 const uint32_t bd = sdesc_lo(k_base + st * C::kTileBytes, 16);
                 const uint32_t d_s = tmem + C::kColS + x * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-                    umma_ss(d_s, sdesc_at(ad, off), sdesc_at(bd, off), C::kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss_w(d_s, sdesc_at(ad, off), sdesc_at(bd, off), C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars.s_full[x]);
-                if (x == 1 || i >= nk1) umma_commit(&bars.k_empty[st]);
+                umma_commit_w(&bars.s_full[x]);
+                if (release_k) umma_commit_w(&bars.k_empty[st]);
+                if (release_q) umma_commit_w(&bars.q_empty[q % C::kQSlots]);
                 return true;
             };
-            for (uint32_t r = 0; ok; ++r) {
-                if (!(ok = mbar_wait_ool(&bars.ring_full[r & 3], (r >> 2) & 1, wd))) break;
-                const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
-                mbar_arrive(&bars.ring_empty[r & 3]);
-                if (idx < 0) break;
-                const ItemGeo gi = decode_item(p, idx);
-                if (gi.n_kv == 0) continue;
-                const int32_t nk[2] = {gi.t[0].n_kv, gi.t[1].n_kv};
-                nk1 = nk[1];
+            auto wait_q = [&](uint32_t q) -> bool {
+                if (!wwait(&bars.q_full[q % C::kQSlots], (q / C::kQSlots) & 1)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // the next ring entry with key tiles to visit: n = 0 once the queue is exhausted
+            // Take the next ring entry with key tiles to visit (n = 0 once the queue is
+            // exhausted).  Blocking, or (poll) only as far as entries are published:
+            // then it returns false with fetched unset when the next one is not there.
+            auto take = [&](int32_t (&nk)[2], int32_t &n, bool poll, bool &fetched) -> bool {
+                fetched = false;
+                while (true) {
+                    if (poll) {
+                        if (!__all_sync(0xffffffffu, mbar_try_wait(&bars.ring_full[r & 3], (r >> 2) & 1))) return true;
+                    } else if (!wwait(&bars.ring_full[r & 3], (r >> 2) & 1)) {
+                        return false;
+                    }
+                    const ItemRec &rc = recs[r & 3];
+                    const int32_t idx = __shfl_sync(0xffffffffu, rc.idx, 0), a = __shfl_sync(0xffffffffu, rc.gi.t[0].n_kv, 0),
+                                  b = __shfl_sync(0xffffffffu, rc.gi.t[1].n_kv, 0), m = __shfl_sync(0xffffffffu, rc.gi.n_kv, 0);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
+                    ++r;
+                    if (idx < 0 || m > 0) {
+                        nk[0] = idx < 0 ? 0 : a;
+                        nk[1] = idx < 0 ? 0 : b;
+                        n = idx < 0 ? 0 : m;
+                        fetched = true;
+                        return true;
+                    }
+                }
+            };
+            int32_t nk[2] = {0, 0}, n = 0;
+            bool pre[2] = {false, false};  // S_x(0) already issued in the previous item's last visit
+            bool fetched = false;
+            ok = take(nk, n, false, fetched);
+            while (ok && n > 0) {
+                // Q ring indices of the item's tiles (A first), as the producer loads them
+                const uint32_t qx[2] = {qi, qi + (nk[0] > 0 ? 1u : 0u)};
+                const uint32_t qn = qx[1] + (nk[1] > 0 ? 1u : 0u);
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
-                    if (nk[x] == 0) continue;
-                    if (!(ok = mbar_wait_ool(&bars.q_full[x], q_it[x] & 1, wd))) break;
-                    tc_fence_after();
-                    if (!(ok = issue_s(x, kv_it, 0))) break;
+                    if (nk[x] == 0 || pre[x]) continue;
+                    if (!(ok = wait_q(qx[x]) && issue_s(x, qx[x], kv_it, x == 1 || nk[1] == 0, nk[x] == 1))) break;
                 }
-                for (int32_t i = 0; i < gi.n_kv && ok; ++i) {
+                int32_t mk[2] = {0, 0}, m = 0;  // the next item
+                bool pre_next[2] = {false, false};
+                fetched = false;
+                for (int32_t i = 0; i < n && ok; ++i) {
                     const uint32_t kvi = kv_it + i;
                     const uint32_t st = kvi % C::kStages;
-                    if (!(ok = mbar_wait_ool(&bars.v_full[st], (kvi / C::kStages) & 1, wd))) break;
+                    if (!(ok = wwait(&bars.v_full[st], (kvi / C::kStages) & 1))) break;
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (i >= nk[x]) continue;
-                        if (!(ok = mbar_wait_ool(&bars.p_full[x], s_it[x] & 1, wd))) break;
-                        if (i == 0 && !(ok = mbar_wait_ool(&bars.o_empty[x], (o_it[x] & 1) ^ 1, wd))) break;
+                        if (!(ok = wwait(&bars.p_full[x], s_it[x] & 1))) break;
+                        if (i == 0 && !(ok = wwait(&bars.o_empty[x], (o_it[x] & 1) ^ 1))) break;
                         tc_fence_after();
                         const uint32_t bd = sdesc_lo(v_base + st * C::kTileBytes, C::kHalfBytes);
                         const uint32_t d_o = tmem + C::kColO + x * D, a_p = tmem + C::kColS + x * 128;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_ts(d_o, a_p + kk * 8, sdesc_at(bd, kk * 2048), C::kIdescPV,
+                            umma_ts_w(d_o, a_p + kk * 8, sdesc_at(bd, kk * 2048), C::kIdescPV,
                                     (i > 0 || kk > 0) ? 1u : 0u);
                         ++s_it[x];
                         if (i + 1 < nk[x]) {
-                            if (!(ok = issue_s(x, kvi + 1, i + 1))) break;
-                        } else {
-                            umma_commit(&bars.o_full[x]);   // O_x complete
-                            umma_commit(&bars.q_empty[x]);  // Q_x no longer read
-                            ++q_it[x];
-                            ++o_it[x];
+                            if (!(ok = issue_s(x, qx[x], kvi + 1, x == 1 || i + 1 >= nk[1], i + 2 == nk[x]))) break;
+                            continue;
+                        }
+                        umma_commit_w(&bars.o_full[x]);  // O_x complete
+                        ++o_it[x];
+                        // Both tiles end here: the next item's S_x(0) takes the place of
+                        // S_x(i+1) when its entry is published and its Q and K tiles have
+                        // landed; otherwise the next item issues it (waiting here would
+                        // hold back PV_B).  Tile B's goes only after tile A's, which the K
+                        // release rule assumes.
+                        if (nk[0] != nk[1]) continue;
+                        if (x == 0 && !(ok = take(mk, m, true, fetched))) break;
+                        const uint32_t q = qn + (x == 1 && mk[0] > 0 ? 1u : 0u);
+                        const uint32_t kn = kv_it + n;
+                        if (fetched && mk[x] > 0 && (x == 0 || mk[0] == 0 || pre_next[0]) &&
+                            __all_sync(0xffffffffu, mbar_try_wait(&bars.q_full[q % C::kQSlots], (q / C::kQSlots) & 1) &&
+                                                        mbar_try_wait(&bars.k_full[kn % C::kStages], (kn / C::kStages) & 1))) {
+                            tc_fence_after();
+                            if (!(ok = issue_s(x, q, kn, x == 1 || mk[1] == 0, mk[x] == 1))) break;
+                            pre_next[x] = true;
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&bars.v_empty[st]);
+                    umma_commit_w(&bars.v_empty[st]);
                 }
-                kv_it += gi.n_kv;
+                if (!ok) break;
+                if (!fetched && !(ok = take(mk, m, false, fetched))) break;
+                pre[0] = pre_next[0];
+                pre[1] = pre_next[1];
+                kv_it += n;
+                qi = qn;
+                nk[0] = mk[0];
+                nk[1] = mk[1];
+                n = m;
             }
-            umma_commit(&bars.mma_done);  // arrives once every MMA issued above has completed
+            umma_commit_w(&bars.mma_done);  // arrives once every MMA issued above has completed
             const DevCtl drain{p.ctl.err, p.ctl.wait_limit_ns};
             uint32_t zero = 0;
             const Watchdog wd2{&drain, &zero};
@@ -434,11 +549,11 @@ __global__ void __launch_bounds__(320, 1)
         for (uint32_t r = 0; ok; ++r) {
             ok = __all_sync(0xffffffffu, mbar_wait_ool(&bars.ring_full[r & 3], (r >> 2) & 1, wd));
             if (!ok) break;
-            const int32_t idx = *reinterpret_cast<volatile int32_t *>(&bars.ring[r & 3]);
+            const int32_t idx = recs[r & 3].idx;
+            const ItemGeo gi = recs[r & 3].gi;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.ring_empty[r & 3]);
             if (idx < 0) break;
-            const ItemGeo gi = decode_item(p, idx);
             const TileGeo tg = gi.t[x];
             const int32_t tok = row / p.G;
             const int32_t h = gi.g * p.G + (row % p.G);
