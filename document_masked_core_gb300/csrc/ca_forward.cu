@@ -55,6 +55,7 @@ struct FwdParams {
     int32_t hq, G, tpt;
     float scale_log2;  // softmax_scale * log2(e)
     void *o;
+    int32_t o_v8;  // O is 32-byte aligned: the epilogue stores whole 32-byte sectors
     float *lse;
     int32_t *sched;  // work-queue counter (zeroed before the launch)
     SplitScratch split;  // partial rows of split items and their row counters (zeroed before the launch)
@@ -681,29 +682,36 @@ __global__ void __launch_bounds__(320, 1)
                                              __uint_as_float(orr[4 * e + 2]) * inv_l,
                                              __uint_as_float(orr[4 * e + 3]) * inv_l);
                 } else if (valid) {
+                    // a lane writes its own row: 16- or 32-byte pieces, each a separate
+                    // sector of the warp's store, so the wider pieces halve the requests
                     if (OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + out_idx * D + c * 32);
+                        float *dst = static_cast<float *>(p.o) + out_idx * D + c * 32;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(orr[4 * e]) * inv_l,
-                                                 __uint_as_float(orr[4 * e + 1]) * inv_l,
-                                                 __uint_as_float(orr[4 * e + 2]) * inv_l,
-                                                 __uint_as_float(orr[4 * e + 3]) * inv_l);
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * inv_l);
+                        if (p.o_v8) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                st_global_v8(dst + 8 * e, orr[8 * e], orr[8 * e + 1], orr[8 * e + 2], orr[8 * e + 3],
+                                             orr[8 * e + 4], orr[8 * e + 5], orr[8 * e + 6], orr[8 * e + 7]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                reinterpret_cast<uint4 *>(dst)[e] =
+                                    make_uint4(orr[4 * e], orr[4 * e + 1], orr[4 * e + 2], orr[4 * e + 3]);
+                        }
                     } else {
-                        uint4 *dst =
-                            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32);
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.o) + out_idx * D + c * 32;
+                        uint32_t w[16];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(orr[8 * e + 0]) * inv_l,
-                                            __uint_as_float(orr[8 * e + 1]) * inv_l);
-                            w.y = pack_bf16(__uint_as_float(orr[8 * e + 2]) * inv_l,
-                                            __uint_as_float(orr[8 * e + 3]) * inv_l);
-                            w.z = pack_bf16(__uint_as_float(orr[8 * e + 4]) * inv_l,
-                                            __uint_as_float(orr[8 * e + 5]) * inv_l);
-                            w.w = pack_bf16(__uint_as_float(orr[8 * e + 6]) * inv_l,
-                                            __uint_as_float(orr[8 * e + 7]) * inv_l);
-                            dst[e] = w;
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv_l, __uint_as_float(orr[2 * e + 1]) * inv_l);
+                        if (p.o_v8) {
+                            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                            st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                reinterpret_cast<uint4 *>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                         }
                     }
                 }
@@ -770,6 +778,7 @@ cudaError_t launch_forward(const ca_plan *pl, const void *q, const void *k, cons
     prm.tpt = pl->tpt;
     prm.scale_log2 = pl->scale * 1.4426950408889634f;
     prm.o = o;
+    prm.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
     prm.lse = lse;
     prm.sched = sched;
     prm.split = split;

@@ -343,6 +343,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// 32-byte global store (one full sector per lane); the address must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3),
+                 "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tcgen05.mma / TMA reads of shared memory).
 __device__ __forceinline__ void fence_view_async_shared() {
