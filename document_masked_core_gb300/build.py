@@ -19,7 +19,8 @@ OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libca.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ca_plan.cpp", "ca_sched.cpp", "ca_forward.cu", "ca_backward.cu", "ca_merge.cu", "ca_noalloc.cu"]
+SOURCES = ["ca_plan.cpp", "ca_sched.cpp", "ca_forward.cu", "ca_backward.cu", "ca_backward_pair.cu", "ca_merge.cu",
+           "ca_noalloc.cu"]
 
 
 def nvcc() -> str:

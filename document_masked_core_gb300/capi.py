@@ -25,11 +25,14 @@ CA_ERR_DEVICE_BOUNDS = 5
 CA_ERR_NO_DEVICE = 6
 CA_DTYPE_BF16 = 0
 CA_DTYPE_FP32 = 1
+CA_BWD_KERNEL_AUTO = 0
+CA_BWD_KERNEL_SINGLE = 1
+CA_BWD_KERNEL_PAIR = 2
 
 # names declared in include/ca.h and include/ca_sched.h, in order
 EXPORTS = [
     "ca_plan_create", "ca_plan_dry_run", "ca_plan_create_masked", "ca_plan_dry_run_masked", "ca_plan_set_kv_split",
-    "ca_plan_info",
+    "ca_plan_set_backward_kernel", "ca_plan_info",
     "ca_plan_task_pairs", "ca_plan_destroy",
     "ca_forward", "ca_backward", "ca_backward_noalloc", "ca_merge", "ca_device_status", "ca_plan_set_wait_limit",
     "ca_watchdog_selftest", "ca_plan_set_timing_events", "ca_status_string", "ca_last_error", "ca_version",
@@ -115,6 +118,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                          ctypes.POINTER(PlanInfo), vp]
     L.ca_plan_set_kv_split.restype = st
     L.ca_plan_set_kv_split.argtypes = [vp, i32]
+    L.ca_plan_set_backward_kernel.restype = st
+    L.ca_plan_set_backward_kernel.argtypes = [vp, i32]
     L.ca_plan_info.restype = st
     L.ca_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
     L.ca_plan_task_pairs.restype = st
@@ -290,6 +295,12 @@ class Plan:
         tiles into parts merged in the launch (0 = automatic, < 0 = never).
         The workspace size may change: allocate it after this call."""
         _check(load().ca_plan_set_kv_split(self.handle, int(visits_per_part)))
+
+    def set_backward_kernel(self, kind: int):
+        """Which backward main kernel runs: CA_BWD_KERNEL_AUTO or
+        CA_BWD_KERNEL_SINGLE (the one-CTA kernel), CA_BWD_KERNEL_PAIR (the
+        CTA-pair kernel where it applies)."""
+        _check(load().ca_plan_set_backward_kernel(self.handle, int(kind)))
 
     def task_pairs(self) -> np.ndarray:
         out = np.zeros(self.n_tasks, dtype=np.int64)

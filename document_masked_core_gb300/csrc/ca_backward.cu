@@ -841,6 +841,15 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
+cudaError_t launch_dq_finalize(const ca_plan *pl, const float *dq_acc, void *dq, cudaStream_t stream) {
+    const int64_t n8 = pl->total_q * pl->hq * pl->d / 8;
+    const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
+    ca_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n8);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = mark(pl, 5, stream);
+    return e;
+}
+
 template <int D>
 cudaError_t launch_main_t(const ca_plan *pl, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &prm,
@@ -892,7 +901,13 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
         if (e == cudaSuccess) e = mark(pl, 3, stream);
         if (e != cudaSuccess) return e;
     }
-    // 2. main pass
+    // 2. main pass: on CTA pairs where the plan selects them
+    if (use_bwd_pair(pl)) {
+        cudaError_t e = launch_bwd_main_pair(pl, q, k, v, d_o, dq_acc, lse, Dvec, sched, dk, dv, stream);
+        if (e == cudaSuccess) e = mark(pl, 4, stream);
+        if (e != cudaSuccess) return e;
+        return launch_dq_finalize(pl, dq_acc, dq, stream);
+    }
     CUtensorMap tq, tk, tv, tdo, tdq;
     if (make_tmap_3d(&tq, q, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt) != CA_OK ||
         make_tmap_3d(&tdq, dq_acc, pl->total_q, pl->hq, pl->d, pl->G, pl->tpt, true) != CA_OK ||
@@ -925,14 +940,7 @@ cudaError_t launch_backward(const ca_plan *pl, const void *q, const void *k, con
     if (e == cudaSuccess) e = mark(pl, 4, stream);
     if (e != cudaSuccess) return e;
     // 3. dQ accumulator -> bf16
-    {
-        const int64_t n8 = units * pl->d / 8;
-        const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
-        ca_bwd_dq_kernel<<<blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16 *>(dq), n8);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) e = mark(pl, 5, stream);
-    return e;
+    return launch_dq_finalize(pl, dq_acc, dq, stream);
 }
 
 }  // namespace ca

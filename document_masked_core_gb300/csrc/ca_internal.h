@@ -121,6 +121,42 @@ __host__ __device__ inline void key_tile_rows(const DevTask &t, int32_t k0, int3
     }
 }
 
+// Query tiles (of tpt tokens) of task t whose rows see key tile jt: the rows
+// of key_tile_rows inside the task, as a first tile and a count (0: none).
+__host__ __device__ inline void key_tile_query_tiles(const DevTask &t, int32_t jt, int32_t tpt, int32_t *first,
+                                                     int32_t *count) {
+    *first = 0;
+    *count = 0;
+    int32_t pmin, pmax;
+    key_tile_rows(t, jt * 128, &pmin, &pmax);
+    const int32_t q0 = t.q_start, q1 = t.q_start + t.q_len - 1;  // inclusive
+    const int32_t lo = pmin > q0 ? pmin : q0, hi = pmax < q1 ? pmax : q1;
+    if (lo > hi) return;
+    *first = (lo - q0) / tpt;
+    *count = (hi - q0) / tpt - *first + 1;
+}
+
+// The same for the pair of key tiles 2 jp and 2 jp + 1 that a CTA pair
+// processes together: one range covering both tiles' ranges (a query tile in
+// between that sees neither gets all-zero probabilities and adds nothing).
+__host__ __device__ inline void key_pair_query_tiles(const DevTask &t, int32_t jp, int32_t tpt, int32_t *first,
+                                                     int32_t *count) {
+    int32_t fa, ca, fb, cb;
+    key_tile_query_tiles(t, 2 * jp, tpt, &fa, &ca);
+    key_tile_query_tiles(t, 2 * jp + 1, tpt, &fb, &cb);
+    if (cb == 0) {
+        *first = fa;
+        *count = ca;
+    } else if (ca == 0) {
+        *first = fb;
+        *count = cb;
+    } else {
+        const int32_t lo = fa < fb ? fa : fb, hi = fa + ca > fb + cb ? fa + ca : fb + cb;
+        *first = lo;
+        *count = hi - lo;
+    }
+}
+
 // Forward item: query tiles `tile` and `tile + 1` (tile even; tokens
 // [tile*T, tile*T+2T) of the task, T = 128 / G) of kv head g, processed
 // together by one CTA, over visits [i0, i1) of the pair's key-tile sequence
@@ -134,7 +170,9 @@ struct FwdItem {
 };
 
 // Backward tile: key tile kv_tile of document doc, kv head g; n_q = number of
-// query tiles (over all tasks of the document) that see it.
+// query tiles (over all tasks of the document) that see it.  In the list of
+// the CTA-pair kernel, kv_tile is the pair index jp (key tiles 2 jp, 2 jp + 1)
+// and n_q counts the query tiles of key_pair_query_tiles.
 struct BwdItem {
     int32_t doc, g, kv_tile, n_q;
 };
@@ -161,6 +199,8 @@ struct ca_plan {
     std::vector<int64_t> task_pairs;
     std::vector<ca::DevTask> h_tasks;
     int64_t n_fwd = 0, n_bwd = 0;
+    int64_t n_bwd_pair = 0;               // items of the CTA-pair backward (0: not applicable)
+    int32_t bwd_kernel = 0;               // CA_BWD_KERNEL_*: which backward main kernel runs
     int64_t workspace_bytes = 0;
     int32_t kv_split = 0;                 // 0: automatic, < 0: never split, > 0: visits per part
     int64_t n_split = 0, n_slots = 0;     // split pairs, partial slots (256 rows each)
@@ -172,6 +212,7 @@ struct ca_plan {
     ca::DevTask *d_tasks = nullptr;
     ca::FwdItem *d_fwd = nullptr;
     ca::BwdItem *d_bwd = nullptr;
+    ca::BwdItem *d_bwd_pair = nullptr;
     int32_t *d_doc_task_ptr = nullptr;  // [n_docs + 1] CSR into d_doc_tasks
     int32_t *d_doc_tasks = nullptr;     // task ids grouped by document
     int32_t *d_doc_info = nullptr;      // [n_docs][2] = {kv_off, doc_len}
@@ -235,6 +276,12 @@ cudaError_t launch_forward(const ca_plan *p, const void *q, const void *k, const
 cudaError_t launch_backward(const ca_plan *p, const void *q, const void *k, const void *v, const void *o,
                             const float *lse, const void *d_o, void *dq, void *dk, void *dv,
                             void *workspace, cudaStream_t stream);
+// Backward main pass on CTA pairs (head_dim 128, G dividing 64): see ca_backward_pair.cu.
+cudaError_t launch_bwd_main_pair(const ca_plan *p, const void *q, const void *k, const void *v, const void *d_o,
+                                 float *dq_acc, const float *lse, const float *Dvec, int32_t *sched, void *dk,
+                                 void *dv, cudaStream_t stream);
+// Whether the plan's backward runs the CTA-pair main kernel (selected and applicable).
+inline bool use_bwd_pair(const ca_plan *p) { return p->n_bwd_pair > 0 && p->bwd_kernel == CA_BWD_KERNEL_PAIR; }
 cudaError_t launch_merge(int32_t n_parts, const void *const *o_parts, const float *const *lse_parts,
                          int32_t parts_dtype, int64_t rows, int32_t heads, int32_t head_dim, void *o_out,
                          int32_t out_dtype, float *lse_out, cudaStream_t stream);

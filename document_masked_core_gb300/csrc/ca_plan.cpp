@@ -172,6 +172,7 @@ void free_device(ca_plan *p) {
     cudaFree(p->d_tasks);
     cudaFree(p->d_fwd);
     cudaFree(p->d_bwd);
+    cudaFree(p->d_bwd_pair);
     cudaFree(p->d_doc_task_ptr);
     cudaFree(p->d_doc_tasks);
     cudaFree(p->d_doc_info);
@@ -179,6 +180,7 @@ void free_device(ca_plan *p) {
     p->d_tasks = nullptr;
     p->d_fwd = nullptr;
     p->d_bwd = nullptr;
+    p->d_bwd_pair = nullptr;
     p->d_doc_task_ptr = nullptr;
     p->d_doc_tasks = nullptr;
     p->d_doc_info = nullptr;
@@ -341,6 +343,7 @@ struct HostPlan {
     ca_plan *p = nullptr;
     FwdList fwd;
     std::vector<BwdItem> bwd;
+    std::vector<BwdItem> bwd_pair;  // items of the CTA-pair backward (head_dim 128, G divides 64)
     std::vector<int32_t> ptr, dtasks, doc_info;
 };
 
@@ -466,14 +469,31 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
             p->bwd_tile_pairs += static_cast<int64_t>(nq) * p->hkv;
         }
     }
+    // The CTA-pair kernel's items: pairs of key tiles (2 jp, 2 jp + 1), the
+    // second past the document's end when it has an odd number of tiles.
+    std::vector<BwdItem> &bwd_pair = hp->bwd_pair;
+    if (p->d == 128 && 64 % p->G == 0) {
+        for (int32_t i = 0; i < n_docs; ++i) {
+            const int32_t nkt = static_cast<int32_t>((doc_len[i] + kTileKeys - 1) / kTileKeys);
+            for (int32_t jp = 0; 2 * jp < nkt; ++jp) {
+                int32_t nq = 0;
+                for (int32_t k = ptr[i]; k < ptr[i + 1]; ++k) {
+                    int32_t f, c;
+                    key_pair_query_tiles(p->h_tasks[dtasks[k]], jp, p->tpt, &f, &c);
+                    nq += c;
+                }
+                for (int32_t g = 0; g < p->hkv; ++g) bwd_pair.push_back({i, g, jp, nq});
+            }
+        }
+    }
     // Group the items of one (document, kv head): CTAs that run at the same
     // time then add into the same rows of the fp32 dQ accumulator, which keeps
     // that working set (document length x G x head_dim x 4 bytes) in L2.
     // Groups with the most work first; longest items first inside a group.
-    {
+    for (std::vector<BwdItem> *list : {&bwd, &bwd_pair}) {
         std::vector<int64_t> group_work(static_cast<size_t>(n_docs) * p->hkv, 0);
-        for (const BwdItem &b : bwd) group_work[static_cast<size_t>(b.doc) * p->hkv + b.g] += b.n_q;
-        std::stable_sort(bwd.begin(), bwd.end(), [&](const BwdItem &a, const BwdItem &b) {
+        for (const BwdItem &b : *list) group_work[static_cast<size_t>(b.doc) * p->hkv + b.g] += b.n_q;
+        std::stable_sort(list->begin(), list->end(), [&](const BwdItem &a, const BwdItem &b) {
             const int64_t wa = group_work[static_cast<size_t>(a.doc) * p->hkv + a.g];
             const int64_t wb = group_work[static_cast<size_t>(b.doc) * p->hkv + b.g];
             if (wa != wb) return wa > wb;
@@ -483,7 +503,9 @@ ca_status_t build_host_plan(const ca_task_t *tasks, const ca_mask_t *masks, int3
         });
     }
     p->n_bwd = static_cast<int64_t>(bwd.size());
-    if (p->n_bwd > kI32Max) return fail(CA_ERR_UNSUPPORTED, "the backward work list exceeds 2^31 items");
+    p->n_bwd_pair = static_cast<int64_t>(bwd_pair.size());
+    if (p->n_bwd > kI32Max || p->n_bwd_pair > kI32Max)
+        return fail(CA_ERR_UNSUPPORTED, "the backward work list exceeds 2^31 items");
 
     set_workspace_bytes(p);
     return CA_OK;
@@ -622,6 +644,7 @@ ca_status_t ca_plan_create_masked(const ca_task_t *tasks, const ca_mask_t *masks
     cudaStream_t s = static_cast<cudaStream_t>(upload_stream);
     if ((e = upload(&p->d_tasks, p->h_tasks, s)) != cudaSuccess ||
         (e = upload(&p->d_fwd, hp.fwd.items, s)) != cudaSuccess || (e = upload(&p->d_bwd, hp.bwd, s)) != cudaSuccess ||
+        (e = upload(&p->d_bwd_pair, hp.bwd_pair, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_task_ptr, hp.ptr, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_tasks, hp.dtasks, s)) != cudaSuccess ||
         (e = upload(&p->d_doc_info, hp.doc_info, s)) != cudaSuccess ||
@@ -657,6 +680,14 @@ void ca_plan_destroy(ca_plan_t *p) {
     free_device(p);
     if (switched) cudaSetDevice(cur);
     delete p;
+}
+
+ca_status_t ca_plan_set_backward_kernel(ca_plan_t *p, int32_t kind) {
+    if (!p) return fail(CA_ERR_INVALID_ARG, "plan is NULL");
+    if (kind != CA_BWD_KERNEL_AUTO && kind != CA_BWD_KERNEL_SINGLE && kind != CA_BWD_KERNEL_PAIR)
+        return fail(CA_ERR_INVALID_ARG, "unknown backward kernel kind " + std::to_string(kind));
+    p->bwd_kernel = kind;
+    return CA_OK;
 }
 
 ca_status_t ca_plan_set_wait_limit(ca_plan_t *p, int64_t ns) {

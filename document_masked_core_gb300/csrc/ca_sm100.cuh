@@ -325,6 +325,160 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------ CTA pairs
+// A cluster of two CTAs on neighbouring SMs sharing tcgen05 products
+// (cta_group::2): rank 0 issues the pair's MMAs, each CTA holds half of every
+// operand and of every accumulator (PTX ISA, tcgen05 "CTA pair").
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs: release this CTA's earlier writes, acquire the peer's.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive (release at cluster scope) on a barrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// The same arrival with CTA-scope release (ordering only this CTA's earlier
+// accesses, the default of the instruction).
+__device__ __forceinline__ void mbar_arrive_cl_cta(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// One arrival per warp on a cluster-addressed barrier (all 32 lanes converged).
+__device__ __forceinline__ void mbar_arrive_warp_cl(uint32_t cl_addr) {
+    __syncwarp();
+    if ((threadIdx.x & 31u) == 0) mbar_arrive_cl(cl_addr);
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cl_addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cl_addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_b32(uint32_t cl_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+// Make this thread's generic-proxy writes to the shared memory of any CTA of
+// the cluster visible to the async proxy (tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_view_async_cluster() {
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// Bounded waits with cluster-scope acquire, for barriers that receive
+// arrivals from the peer CTA or from the pair's tcgen05 commits.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_try_wait_sleep_cl(uint64_t *bar, uint32_t parity) {
+    if constexpr (kHintNs == 0) {
+        return mbar_try_wait_cl(bar, parity);
+    } else {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "n"(kHintNs)
+            : "memory");
+        return ok != 0;
+    }
+}
+// kHintNs: the suspend-time hint of the polls after the first (0: plain polls).
+template <uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity, const Watchdog &wd) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_sleep_cl<kHintNs>(bar, parity)) return true;
+        if (*wd.abort_flag) return false;
+        if (globaltimer() - t0 > wd.ctl->wait_limit_ns) {
+            *wd.abort_flag = 1u;
+            atomicOr(wd.ctl->err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// TMA tile load into this CTA's shared memory whose byte count is signalled on
+// the barrier at cluster address bar_cl, which may be the peer CTA's.
+__device__ __forceinline__ void tma_load_3d_pair(void *smem_dst, const CUtensorMap *map, uint32_t bar_cl, int32_t c0,
+                                                 int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// TMEM of a CTA pair: one warp of each CTA allocates; the pair's columns are
+// the same in both CTAs.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Pair products, issued by rank 0: the descriptors and TMEM addresses apply
+// in both CTAs.
+__device__ __forceinline__ void umma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at bar's offset in both CTAs of the pair once every
+// pair product issued so far by this thread completes.
+__device__ __forceinline__ void umma_pair_commit_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+// The same, on this CTA's barrier only.
+__device__ __forceinline__ void umma_pair_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ math
 __device__ __forceinline__ float ex2(float x) {
     float y;

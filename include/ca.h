@@ -16,10 +16,10 @@
  * are detected on the host before any launch and returned as a status; the
  * library never aborts the process.  Functions are safe to call from several
  * host threads on distinct plans; one plan may be used concurrently on
- * several streams if each call has its own workspace.  Three calls change a
- * plan -- ca_plan_set_kv_split, ca_plan_set_wait_limit and
- * ca_plan_set_timing_events -- and must not race with any other call on the
- * same plan from another host thread.  Every call that takes a plan needs
+ * several streams if each call has its own workspace.  Four calls change a
+ * plan -- ca_plan_set_kv_split, ca_plan_set_backward_kernel,
+ * ca_plan_set_wait_limit and ca_plan_set_timing_events -- and must not race
+ * with any other call on the same plan from another host thread.  Every call that takes a plan needs
  * the device the plan was created on to be current (CA_ERR_INVALID_ARG
  * otherwise, before any launch).
  *
@@ -188,6 +188,26 @@ ca_status_t ca_plan_dry_run_masked(const ca_task_t *tasks, const ca_mask_t *mask
  * may use the plan meanwhile.
  */
 ca_status_t ca_plan_set_kv_split(ca_plan_t *plan, int32_t visits_per_part);
+
+/*
+ * Which backward main kernel a plan's ca_backward / ca_backward_noalloc run.
+ * CA_BWD_KERNEL_AUTO (every plan's default) and CA_BWD_KERNEL_SINGLE: the
+ * one-CTA kernel (one SM per 128-key tile).  CA_BWD_KERNEL_PAIR: where it
+ * applies (head_dim 128 and a number of query heads per kv head that divides
+ * 64), the CTA-pair kernel, which processes two neighbouring key tiles of a
+ * document on the two SMs of a cluster with tcgen05 pair products (each SM
+ * reads half of every product's shared-memory B operand and reduces half of
+ * each query tile's dQ) and exchanges dS rows between the two SMs; elsewhere
+ * the one-CTA kernel.  On a GB300 the pair kernel is the slower of the two
+ * (about 1.5x on the 64K packed chunk), which is why AUTO does not select it.
+ * Both compute the same definition (Efficient Long-context Language Model
+ * Training by Core Attention Disaggregation, §3.2 "Information flow (backward
+ * pass)"); dK and dV are equal bit for bit, dQ to fp32 summation order.  It
+ * changes the plan: no other host thread may use the plan meanwhile.
+ * CA_ERR_INVALID_ARG for an unknown kind.
+ */
+enum { CA_BWD_KERNEL_AUTO = 0, CA_BWD_KERNEL_SINGLE = 1, CA_BWD_KERNEL_PAIR = 2 };
+ca_status_t ca_plan_set_backward_kernel(ca_plan_t *plan, int32_t kind);
 
 /* Sizes and integer accounting of a plan (all exact, int64). */
 ca_status_t ca_plan_info(const ca_plan_t *plan, ca_plan_info_t *out);

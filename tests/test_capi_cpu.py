@@ -40,6 +40,11 @@ def test_library_exports_every_declared_symbol():
     assert sorted(capi.EXPORTS) == names
 
 
+def test_set_backward_kernel_needs_a_plan():
+    L = capi.load()
+    assert L.ca_plan_set_backward_kernel(None, capi.CA_BWD_KERNEL_PAIR) == capi.CA_ERR_INVALID_ARG
+
+
 def test_status_strings_and_version():
     L = capi.load()
     for s in range(7):

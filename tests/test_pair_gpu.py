@@ -1,0 +1,118 @@
+"""GPU parity of the CTA-pair backward main kernel (ca_plan_set_backward_kernel
+with CA_BWD_KERNEL_PAIR): against the fp64 oracle on small cases, and against
+the one-CTA kernel on the same inputs -- dK and dV bit for bit (both
+accumulate the same products in the same order; query tiles that see only one
+of the pair's key tiles add exact zeros to the other), dQ to fp32 summation
+order (the reduce-adds land in a different order)."""
+import numpy as np
+import pytest
+import torch
+
+import document_masked_core_gb300 as ca
+import oracle
+import workloads as W
+from cases import EDGE
+from parity import check_grad, rel_fro, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from document_masked_core_gb300 import build
+    build.build()
+
+
+def pair_applies(w):
+    G = w.num_q_heads // w.num_kv_heads
+    return w.head_dim == 128 and 64 % G == 0
+
+
+SMALL = [w for w in EDGE if pair_applies(w)] + [
+    # odd numbers of key tiles: the last pair's second tile lies past the document
+    W.custom("pair_odd_tiles", [384, 129, 1000], [(i, 0, l, 0, l) for i, l in enumerate([384, 129, 1000])],
+             hq=32, hkv=8, d=128, seed=11),
+    # G = 1, 2, 64: 128, 64 and 2 query tokens per tile, 64, 32 and 1 per CTA of the pair
+    W.custom("pair_g1", [700, 300], [(0, 0, 700, 0, 700), (1, 0, 300, 0, 300)], hq=2, hkv=2, d=128, seed=12),
+    W.custom("pair_g2", [500], [(0, 0, 500, 0, 500)], hq=4, hkv=2, d=128, seed=13),
+    W.custom("pair_g64", [90, 200], [(0, 0, 90, 0, 90), (1, 0, 200, 0, 200)], hq=64, hkv=1, d=128, seed=14),
+    # sparse masks: sink + window narrower than a tile, a sliding window, causal blockwise
+    W.custom("pair_window40", [1500], [(0, 0, 1500, 0, 1500)], hq=32, hkv=8, d=128, seed=15, masks=[(0, 0, 40)]),
+    W.custom("pair_lambda", [2500, 700], [(0, 0, 2500, 0, 2500), (1, 0, 700, 0, 700)], hq=32, hkv=8, d=128, seed=16,
+             masks=[(64, 0, 512), (64, 0, 512)]),
+    W.blockwise_chunk(seed=17, total=2048, block=256),
+]
+
+
+def fwd_bwd_both(w, inputs=None):
+    if inputs is None:
+        inputs = W.make_tensors(w, device="cuda")
+    torch.cuda.synchronize()
+    q, k, v, do = inputs
+    plan = ca.Plan.from_workload(w)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    out = {}
+    for kind in (ca.capi.CA_BWD_KERNEL_SINGLE, ca.capi.CA_BWD_KERNEL_PAIR):
+        plan.set_backward_kernel(kind)
+        dq, dk, dv = ca.alloc_backward(plan)
+        dq.fill_(float("nan"))
+        dk.fill_(7.0)
+        dv.fill_(7.0)
+        plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        out[kind] = (dq, dk, dv)
+    return (q, k, v, do), out[ca.capi.CA_BWD_KERNEL_SINGLE], out[ca.capi.CA_BWD_KERNEL_PAIR]
+
+
+def doc_rows(w):
+    rows = np.zeros(w.total_kv, dtype=bool)
+    for off, L in zip(w.doc_kv_offset, w.doc_len):
+        rows[int(off):int(off + L)] = True
+    return rows
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_pair_backward_matches_oracle_and_single(w):
+    (q, k, v, do), single, pair = fwd_bwd_both(w)
+    dq, dk, dv = pair
+    dQ, dK, dV = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    inside = doc_rows(w)
+    check_grad(to64(dq), dQ, "dQ")
+    check_grad(to64(dk)[inside], dK[inside], "dK")
+    check_grad(to64(dv)[inside], dV[inside], "dV")
+    # rows outside every document are not written
+    assert np.all(to64(dk)[~inside] == 7.0) and np.all(to64(dv)[~inside] == 7.0)
+    assert torch.equal(dk, single[1]) and torch.equal(dv, single[2])
+    assert rel_fro(to64(dq), to64(single[0])) <= 1e-4
+
+
+def test_pair_backward_equals_single_on_the_64k_chunk():
+    """The bench workload at full size: every dK and dV bit for bit, dQ to
+    summation order (the one-CTA kernel is compared with the oracle on every
+    row and column of this chunk elsewhere)."""
+    w = W.llama8b_chunk(seed=0)
+    _, single, pair = fwd_bwd_both(w)
+    assert torch.equal(pair[1], single[1]) and torch.equal(pair[2], single[2])
+    assert bool(torch.isfinite(pair[0]).all())
+    a, b = pair[0].double(), single[0].double()
+    assert float((a - b).norm() / b.norm()) <= 1e-4
+
+
+def test_pair_selection_falls_back_where_it_does_not_apply():
+    """head_dim 64 or G = 128: CA_BWD_KERNEL_PAIR runs the one-CTA kernel."""
+    for w in (W.tiny_chunk(), [x for x in EDGE if x.name == "g128_d128"][0]):
+        assert not pair_applies(w)
+        _, single, pair = fwd_bwd_both(w)
+        assert torch.equal(pair[1], single[1]) and torch.equal(pair[2], single[2])
+        assert rel_fro(to64(pair[0]), to64(single[0])) <= 1e-4
+
+
+def test_set_backward_kernel_rejects_unknown_kinds():
+    plan = ca.Plan.from_workload(W.tiny_chunk())
+    with pytest.raises(ca.CAError):
+        plan.set_backward_kernel(3)
+    with pytest.raises(ca.CAError):
+        plan.set_backward_kernel(-1)
