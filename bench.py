@@ -275,7 +275,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_step):
+def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_step, step_ms):
     """The same step through the C ABI with host buffers: pinned host -> device
     copies of Q, K, V, dO and device -> host copies of O, LSE, dQ, dK, dV inside
     the timed region, every step.
@@ -362,8 +362,9 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
 
     warm = max(1, args.warmup // 2)
     # the overlapped region holds one pipeline fill (the first copy in) and one drain (the last copy
-    # out), about 13 ms together; a training loop pays them once, so the region is at least 60 steps
-    n_e2e = max(args.steps, 60)
+    # out), about 13 ms together; a training loop pays them once, so the region runs as long as the
+    # sustained region (at least 60 steps)
+    n_e2e = max(args.steps, 60, int(np.ceil(args.sustained_s * 1e3 / step_ms)))
     timed(lambda: [serial_step() for _ in range(warm)])
     barrier(world)
     serial_ms = max_over_ranks(timed(lambda: [serial_step() for _ in range(args.steps)]) / args.steps, world)
@@ -380,6 +381,42 @@ def measure_e2e(args, plan, stream, inputs, fwd_out, grads, ws, world, flops_ste
                         "during step k's compute",
             "serial_ms_per_step": serial_ms,
             "serial_value": flops_step * world / (serial_ms * 1e-3) / 1e12}
+
+
+def measure_pair_backward(plan, stream, inputs, fwd_out, grads, ws, info, steps=4):
+    """The backward main kernel on CTA pairs (CA_BWD_KERNEL_PAIR) against the
+    default one-CTA kernel, each timed by the library's own events around the
+    main launch, alternating; the plan is left on its default afterwards."""
+    import torch
+
+    from document_masked_core_gb300 import capi
+    q, k, v, do = inputs
+    o, lse = fwd_out
+    dq, dk, dv = grads
+    sh = stream.cuda_stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record(stream)
+    t = {capi.CA_BWD_KERNEL_SINGLE: [], capi.CA_BWD_KERNEL_PAIR: []}
+    for r in range(2 * steps + 2):
+        kind = (capi.CA_BWD_KERNEL_SINGLE, capi.CA_BWD_KERNEL_PAIR)[r % 2]
+        plan.set_backward_kernel(kind)
+        plan.set_timing_events(ev)
+        with torch.cuda.stream(stream):
+            plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws, stream=sh)
+        stream.synchronize()
+        plan.set_timing_events(None)
+        if r >= 2:  # the first of each is a warm-up
+            t[kind].append(ev[3].elapsed_time(ev[4]))
+    plan.set_backward_kernel(capi.CA_BWD_KERNEL_AUTO)
+    if plan.device_status(stream=sh) != 0:
+        raise RuntimeError("device error in the pair-kernel comparison")
+    single = float(np.median(t[capi.CA_BWD_KERNEL_SINGLE]))
+    pair = float(np.median(t[capi.CA_BWD_KERNEL_PAIR]))
+    return {"single_main_ms": single, "pair_main_ms": pair,
+            "single_main_tflops": info["flops_bwd"] / (single * 1e-3) / 1e12,
+            "pair_main_tflops": info["flops_bwd"] / (pair * 1e-3) / 1e12,
+            "note": "opt-in kernel (ca_plan_set_backward_kernel), not the default; same work, same counted FLOPs"}
 
 
 def measure_masks(args, dev, stream, causal_pairs):
@@ -679,6 +716,7 @@ def run_gpu(args, rank, world, local):
     t0 = time.perf_counter()
     plan = ca.Plan.from_workload(w, stream=stream)
     plan_ms = (time.perf_counter() - t0) * 1e3
+    plan.set_backward_kernel({"auto": 0, "single": 1, "pair": 2}[args.backward_kernel])
     info = plan.info()
     ws = torch.empty(max(16, info["workspace_bytes"]), dtype=torch.uint8, device=dev)
     o, lse = ca.alloc_forward(plan, device=dev)
@@ -757,7 +795,14 @@ def run_gpu(args, rank, world, local):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, plan, stream, (q, k, v, do), (o, lse), (dq, dk, dv), ws, world, flops_step)
+        e2e = measure_e2e(args, plan, stream, (q, k, v, do), (o, lse), (dq, dk, dv), ws, world, flops_step,
+                          ms_local)
+
+    # the opt-in CTA-pair backward main kernel on the same chunk, for comparison (not the headline)
+    pair = None
+    if not args.no_more_configs and w.head_dim == 128:
+        pair = measure_pair_backward(plan, stream, (q, k, v, do), (o, lse), (dq, dk, dv), ws, info)
+        plan.set_backward_kernel({"auto": 0, "single": 1, "pair": 2}[args.backward_kernel])
 
     pk, pk_kind = peaks()
     split_kv = None
@@ -820,6 +865,7 @@ def run_gpu(args, rank, world, local):
                 "l2": (f"inputs larger than L2 (Q and dO {q.numel() * 2 >> 20} MiB, K and V "
                        f"{k.numel() * 2 >> 20} MiB each; L2 is 129 MB)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "backward_kernel": args.backward_kernel,
                 "plan_ms": plan_ms,
             },
             "pct_of_peak": {"burst": 100.0 * value / world / peak, "sustained": 100.0 * value / world / peak_sus,
@@ -833,8 +879,10 @@ def run_gpu(args, rank, world, local):
                          "bwd_dq_finalize": fin_ms},
             "parts_tflops": {"forward": info["flops_fwd"] / (fwd_ms * 1e-3) / 1e12,
                              "backward": info["flops_bwd"] / ((pre_ms + main_ms + fin_ms) * 1e-3) / 1e12},
-            "roofline": {"kernel": "ca_bwd_main_kernel", "bound": "tensor", "achieved": main_tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": measured_traffic(),
+            "roofline": {"kernel": "ca_bwd_pair_kernel" if args.backward_kernel == "pair" else "ca_bwd_main_kernel",
+                         "bound": "tensor", "achieved": main_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": main_tf / peak,
+                         "traffic": None if args.backward_kernel == "pair" else measured_traffic(),
                          "traffic_unit": "bytes per launch (ncu dram read + write, profiles/)",
                          "peak_kind": f"bf16 burst, {pk_kind}",
                          "algorithmic": "8*head_dim*H_q*causal_pairs per launch"},
@@ -851,6 +899,7 @@ def run_gpu(args, rank, world, local):
             "decode": decode,
             "sustained": sustained,
             "more_configs": more or None,
+            "backward_pair_kernel": pair,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
@@ -877,6 +926,8 @@ def main():
     ap.add_argument("--sustained-s", type=float, default=2.5, help="length of the sustained region (seconds)")
     ap.add_argument("--no-more-configs", action="store_true",
                     help="skip the rebatched-pool and 512K-chunk measurements")
+    ap.add_argument("--backward-kernel", choices=["auto", "single", "pair"], default="auto",
+                    help="backward main kernel of the headline step (ca_plan_set_backward_kernel)")
     ap.add_argument("--tokens", type=int, default=65536,
                     help="chunk size (65536 = the measured workload; smaller sizes only for profiling captures)")
     args = ap.parse_args()
