@@ -116,3 +116,78 @@ def test_set_backward_kernel_rejects_unknown_kinds():
         plan.set_backward_kernel(3)
     with pytest.raises(ca.CAError):
         plan.set_backward_kernel(-1)
+
+
+def test_pair_backward_with_float32_o():
+    """The preprocess reads a float32 O; the pair kernel is the same."""
+    w = [x for x in EDGE if x.name == "g8_shards_blocks"][0]
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    torch.cuda.synchronize()
+    plan = ca.Plan.from_workload(w, o_dtype=ca.CA_DTYPE_FP32)
+    plan.set_backward_kernel(ca.capi.CA_BWD_KERNEL_PAIR)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    dq, dk, dv = ca.alloc_backward(plan)
+    plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    dQ, dK, dV = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    inside = doc_rows(w)
+    check_grad(to64(dq), dQ, "dQ")
+    check_grad(to64(dk)[inside], dK[inside], "dK")
+    check_grad(to64(dv)[inside], dV[inside], "dV")
+
+
+def test_pair_backward_replays_from_a_cuda_graph():
+    """Forward + pair backward captured into a CUDA graph replay with the
+    eager results (dK, dV bit for bit, dQ within the gradient tolerance of the
+    oracle), twice in a row."""
+    w = [x for x in SMALL if x.name == "pair_odd_tiles"][0]  # odd numbers of key tiles per document
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    torch.cuda.synchronize()
+    plan = ca.Plan.from_workload(w)
+    plan.set_backward_kernel(ca.capi.CA_BWD_KERNEL_PAIR)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    dq, dk, dv = ca.alloc_backward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    plan.backward(q, k, v, o, lse, do, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    o2, lse2 = ca.alloc_forward(plan)
+    dq2, dk2, dv2 = ca.alloc_backward(plan)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.forward(q, k, v, o2, lse2, ws)
+        plan.backward(q, k, v, o2, lse2, do, dq2, dk2, dv2, ws)
+    ref = oracle.backward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu(), do.cpu()))
+    for _ in range(2):
+        for t in (dq2, dk2, dv2):
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert torch.equal(dk2, dk) and torch.equal(dv2, dv)
+        check_grad(to64(dq2), ref[0], "dQ (graph replay)")
+
+
+def test_pair_backward_without_a_workspace():
+    """ca_backward_noalloc with the pair kernel selected gives the workspace
+    call's dK, dV bit for bit and its dQ to summation order."""
+    w = [x for x in EDGE if x.name == "g8_shards_blocks"][0]
+    q, k, v, do = W.make_tensors(w, device="cuda")
+    torch.cuda.synchronize()
+    plan = ca.Plan.from_workload(w)
+    plan.set_backward_kernel(ca.capi.CA_BWD_KERNEL_PAIR)
+    ws = ca.workspace(plan)
+    o, lse = ca.alloc_forward(plan)
+    plan.forward(q, k, v, o, lse, ws)
+    ref = ca.alloc_backward(plan)
+    plan.backward(q, k, v, o, lse, do, *ref, ws)
+    out = ca.alloc_backward(plan)
+    plan.backward_noalloc(q, k, v, o, lse, do, *out)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert torch.equal(out[1], ref[1]) and torch.equal(out[2], ref[2])
+    assert rel_fro(to64(out[0]), to64(ref[0])) <= 1e-4
