@@ -89,11 +89,13 @@ def test_pair_backward_matches_oracle_and_single(w):
     assert rel_fro(to64(dq), to64(single[0])) <= 1e-4
 
 
-def test_pair_backward_equals_single_on_the_64k_chunk():
-    """The bench workload at full size: every dK and dV bit for bit, dQ to
-    summation order (the one-CTA kernel is compared with the oracle on every
-    row and column of this chunk elsewhere)."""
-    w = W.llama8b_chunk(seed=0)
+@pytest.mark.parametrize("make", [lambda: W.llama8b_chunk(seed=0), lambda: W.rebatched_pool(seed=0)],
+                         ids=["llama8b_chunk_64k", "rebatched_pool_128k"])
+def test_pair_backward_equals_single_at_full_size(make):
+    """The bench workload and the rebatched pool of shards at full size: every
+    dK and dV bit for bit, dQ to summation order (the one-CTA kernel is
+    compared with the oracle on every row and column of these elsewhere)."""
+    w = make()
     _, single, pair = fwd_bwd_both(w)
     assert torch.equal(pair[1], single[1]) and torch.equal(pair[2], single[2])
     assert bool(torch.isfinite(pair[0]).all())
