@@ -115,7 +115,7 @@ struct TileGeo {
 
 // Key tiles of an item: the sequence of key_tile_ranges over the rows of its
 // two query tiles; tile x visits the prefix of n_kv(x) entries that reaches
-// its last row's last visible key (the same rule as the host plan).
+// the furthest key any of its rows sees (the same rule as the host plan).
 struct ItemGeo {
     int32_t g, kv_off, n_kv, i0;
     int32_t part, nparts, split, slot0;
@@ -152,8 +152,8 @@ __device__ __forceinline__ ItemGeo decode_item(const FwdParams &p, int32_t idx) 
     gi.nparts = it.nparts;
     gi.split = it.split;
     gi.slot0 = it.slot0;
-    const int32_t va = gi.t[0].ntok > 0 ? visits_upto(gi.kr, t, end0) : 0;
-    const int32_t vb = gi.t[1].ntok > 0 ? visits_upto(gi.kr, t, end1) : 0;
+    const int32_t va = gi.t[0].ntok > 0 ? visits_upto(gi.kr, t, gi.t[0].p_first, end0) : 0;
+    const int32_t vb = gi.t[1].ntok > 0 ? visits_upto(gi.kr, t, gi.t[1].p_first, end1) : 0;
     gi.t[0].n_kv = max(0, min(va, it.i1) - it.i0);
     gi.t[1].n_kv = max(0, min(vb, it.i1) - it.i0);
     gi.n_kv = max(gi.t[0].n_kv, gi.t[1].n_kv);

@@ -83,13 +83,26 @@ __host__ __device__ inline KeyTileRanges key_tile_ranges(const DevTask &t, int32
 }
 
 // Number of visits (in the order of key_tile_ranges over rows [p0, p1]) up
-// to and including the last key tile row p1x sees: the prefix of the item's
-// sequence a query tile ending at row p1x needs.
-__host__ __device__ inline int32_t visits_upto(const KeyTileRanges &r, const DevTask &t, int32_t p1x) {
-    const RowKeys k = row_keys(t, p1x);
-    int32_t last = -1;  // last visible key of row p1x
-    if (k.hi > k.r2 && k.hi > k.a) last = k.hi - 1;
-    else if (k.r1 > k.a) last = k.r1 - 1;
+// to and including the furthest key tile any row of [q0x, q1x] sees: the
+// prefix of the item's sequence a query tile with those rows needs.  The
+// furthest key is not always the last row's: a row's window part [r2, hi) is
+// non-empty exactly for rows max(lo, kv_start) <= p <= kv_end + window - 2
+// (no upper end when window = 0; none at all when lo >= kv_end), and hi grows
+// with p, so the furthest window key is that of the last such row in the
+// tile; the sink part's end r1 grows with p, so its furthest key is the last
+// row's.
+__host__ __device__ inline int32_t visits_upto(const KeyTileRanges &r, const DevTask &t, int32_t q0x,
+                                               int32_t q1x) {
+    int32_t last = -1;  // furthest visible key of the rows
+    const int64_t e = static_cast<int64_t>(t.kv_start) + t.kv_len;
+    if (t.lo < e) {
+        const int64_t first_w = t.lo > t.kv_start ? t.lo : t.kv_start;
+        const int64_t last_w = t.win > 0 ? e + t.win - 2 : int64_t(q1x);
+        const int64_t pw = last_w < q1x ? last_w : int64_t(q1x);
+        if (pw >= q0x && pw >= first_w) last = row_keys(t, static_cast<int32_t>(pw)).hi - 1;
+    }
+    const RowKeys k = row_keys(t, q1x);
+    if (k.r1 > k.a && k.r1 - 1 > last) last = k.r1 - 1;
     if (last < 0) return 0;
     const int32_t lt = last / 128;
     int32_t n = 0;

@@ -285,8 +285,8 @@ void build_fwd_items(const ca_plan *p, int32_t kv_split, int32_t num_sms, FwdLis
             const bool has_b = tile + 1 < ntiles;
             const int32_t end1 = has_b ? std::min(p0 + 2 * p->tpt, d.q_start + d.q_len) - 1 : end0;
             const KeyTileRanges r = key_tile_ranges(d, p0, end1);
-            const int32_t na = visits_upto(r, d, end0);
-            const int32_t nb = has_b ? visits_upto(r, d, end1) : 0;
+            const int32_t na = visits_upto(r, d, p0, end0);
+            const int32_t nb = has_b ? visits_upto(r, d, end0 + 1, end1) : 0;
             pairs.push_back({t, tile, na, nb, std::max(na, nb)});
             total_visits += static_cast<int64_t>(std::max(na, nb)) * p->hkv;
             out->fwd_tile_pairs += static_cast<int64_t>(na + nb) * p->hkv;

@@ -1,6 +1,8 @@
 """Small workloads shared by the GPU parity tests: sizes the oracle finishes
 in seconds that still span several tiles, ragged tails and the edge cases of
 the CA-task descriptor."""
+import numpy as np
+
 import workloads as W
 
 EDGE = [
@@ -27,3 +29,47 @@ EDGE = [
 ]
 
 
+
+
+def random_pool(seed: int, max_len: int = 1600, max_rows_x_heads: int = 100_000):
+    """A seeded random CA-task pool: 1-4 documents of log-uniform length (with
+    gaps between them in K/V half the time), each cut into 1-3 query shards
+    that keep a random subset of its rows, some shards with a KV block that
+    starts past 0, and on two pools in five a random (sink, lo, window) mask
+    per task.  G is drawn from 1..128 and head_dim from {64, 128}; documents
+    shrink with the head count so that the oracle stays within seconds."""
+    rng = np.random.default_rng(20_000 + seed)
+    d = int(rng.choice([64, 128]))
+    G = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128]))
+    hkv = 1 if G >= 64 else int(rng.choice([1, 2]))
+    hq = G * hkv
+    n_docs = int(rng.integers(1, 5))
+    cap = int(min(max_len, max(16, max_rows_x_heads // hq // n_docs)))
+    doc_len = np.exp(rng.uniform(0.0, np.log(cap), n_docs)).astype(np.int64) + 1
+    gaps = rng.integers(0, 48, n_docs) if rng.random() < 0.5 else np.zeros(n_docs, dtype=np.int64)
+    off = np.cumsum(gaps + np.concatenate([[0], doc_len[:-1]])).astype(np.int64)
+    tasks = []
+    for doc, L in enumerate(int(x) for x in doc_len):
+        cuts = sorted(set(int(c) for c in rng.integers(1, L, int(rng.integers(0, 3)))) if L > 1 else set())
+        edges = [0] + cuts + [L]
+        for a, b in zip(edges[:-1], edges[1:]):
+            if rng.random() < 0.2 and len(edges) > 2:
+                continue                                   # rows no task asks for
+            kv0 = 0
+            if rng.random() < 0.3:
+                kv0 = int(rng.integers(0, b))                  # a KV block, possibly past some rows
+            kv1 = int(rng.integers(max(kv0 + 1, 1), L + 1)) if rng.random() < 0.3 else b
+            tasks.append((doc, a, b - a, kv0, max(1, kv1 - kv0)))
+    if not tasks:
+        tasks.append((0, 0, int(doc_len[0]), 0, int(doc_len[0])))
+    order = rng.permutation(len(tasks))
+    tasks = [tasks[i] for i in order]
+    masks = None
+    if rng.random() < 0.4:
+        masks = []
+        for doc, *_ in tasks:
+            L = int(doc_len[doc])
+            pick = lambda: int(rng.integers(0, L + 1)) if rng.random() < 0.7 else 0  # noqa: E731
+            masks.append((pick(), pick(), pick()))
+    return W.custom(f"random_pool_{seed}", doc_len, tasks, hq=hq, hkv=hkv, d=d, seed=100 + seed,
+                    doc_kv_offset=off, masks=masks)

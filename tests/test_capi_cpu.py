@@ -12,6 +12,7 @@ import document_masked_core_gb300 as ca
 from document_masked_core_gb300 import build, capi
 import oracle
 import workloads as W
+from cases import random_pool
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -150,6 +151,28 @@ def test_tile_lists_cover_visible_tiles(w):
     ref = tile_pairs_reference(w)
     assert info["fwd_tile_pairs"] == ref
     assert info["bwd_tile_pairs"] == ref
+
+
+@pytest.mark.parametrize("seed", range(64))
+def test_random_pools_accounting_and_tile_lists(seed):
+    """Seeded random pools (shards, KV blocks, gaps between documents, masks,
+    G from 1 to 128): per-task pairs, FLOPs and the backward's tile list equal
+    the oracle's and the enumeration's exactly; the forward's list covers every
+    visible tile, and equals the enumeration on unmasked pools."""
+    w = random_pool(seed)
+    info, pairs = ca.dry_run_workload(w)
+    ref = oracle.task_pairs(w)
+    assert np.array_equal(pairs, ref)
+    assert info["causal_pairs"] == int(ref.sum())
+    assert (info["flops_fwd"], info["flops_bwd"]) == oracle.flops(w)
+    tiles = masked_tile_pairs_reference(w)
+    assert info["bwd_tile_pairs"] == tiles
+    if not w.masked:
+        assert info["fwd_tile_pairs"] == tiles
+    else:
+        G = w.num_q_heads // w.num_kv_heads
+        n_qtiles = sum(-(-int(x) // (128 // G)) for x in w.task_q_len) * w.num_kv_heads
+        assert tiles <= info["fwd_tile_pairs"] <= tiles + n_qtiles
 
 
 def test_invalid_descriptors_rejected():
