@@ -205,6 +205,81 @@ def test_invalid_descriptors_rejected():
         assert ei.value.status == capi.CA_ERR_UNSUPPORTED, b
 
 
+def _descriptor(w):
+    return dict(task_doc=w.task_doc.astype(np.int64).copy(), task_q_start=w.task_q_start.copy(),
+                task_q_len=w.task_q_len.copy(), task_kv_start=w.task_kv_start.copy(),
+                task_kv_len=w.task_kv_len.copy(), doc_len=w.doc_len.copy(), doc_kv_offset=w.doc_kv_offset.copy(),
+                num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                masks=np.stack(w.masks(), axis=1))
+
+
+def _break_one_rule(kw, rng):
+    """Violate exactly one of ca_plan_create's INVALID_ARG rules (include/ca.h)
+    in one randomly chosen task or document; returns the rule's name."""
+    n, nd = len(kw["task_doc"]), len(kw["doc_len"])
+    t = int(rng.integers(n))
+    L = int(kw["doc_len"][kw["task_doc"][t]])
+    rules = ["q_len_zero", "q_len_negative", "q_past_doc", "q_start_negative", "q_start_huge", "kv_len_zero",
+             "kv_past_doc", "kv_start_negative", "doc_id_unknown", "doc_id_negative", "doc_shrunk",
+             "mask_negative", "mask_past_doc", "q_len_huge", "scale_bad"]
+    if nd > 1:
+        rules.append("docs_overlap")
+    rule = str(rng.choice(rules))
+    q0, ql, k0, kl = (int(kw[f][t]) for f in ("task_q_start", "task_q_len", "task_kv_start", "task_kv_len"))
+    if rule == "q_len_zero":
+        kw["task_q_len"][t] = 0
+    elif rule == "q_len_negative":
+        kw["task_q_len"][t] = -int(rng.integers(1, 1 << 40))
+    elif rule == "q_past_doc":
+        kw["task_q_len"][t] = L - q0 + int(rng.integers(1, 100))
+    elif rule == "q_start_negative":
+        kw["task_q_start"][t] = -int(rng.integers(1, 1 << 40))
+    elif rule == "q_start_huge":
+        kw["task_q_start"][t] = (1 << 63) - int(rng.integers(1, 1000))
+    elif rule == "q_len_huge":
+        kw["task_q_len"][t] = (1 << 63) - int(rng.integers(1, 1000))
+    elif rule == "kv_len_zero":
+        kw["task_kv_len"][t] = 0
+    elif rule == "kv_past_doc":
+        kw["task_kv_len"][t] = L - k0 + int(rng.integers(1, 100))
+    elif rule == "kv_start_negative":
+        kw["task_kv_start"][t] = -int(rng.integers(1, 1 << 40))
+    elif rule == "doc_id_unknown":
+        kw["task_doc"][t] = nd + int(rng.integers(0, 5))
+    elif rule == "doc_id_negative":
+        kw["task_doc"][t] = -int(rng.integers(1, 5))
+    elif rule == "doc_shrunk":  # the document ends before one of its tasks
+        d = int(kw["task_doc"][t])
+        kw["doc_len"][d] = max(q0 + ql, k0 + kl) - 1
+        if kw["doc_len"][d] < 1:
+            kw["task_q_start"][t] = kw["doc_len"][d] = 1
+    elif rule == "mask_negative":
+        kw["masks"][t, int(rng.integers(3))] = -int(rng.integers(1, 100))
+    elif rule == "mask_past_doc":
+        kw["masks"][t, int(rng.integers(3))] = L + int(rng.integers(1, 100))
+    elif rule == "scale_bad":
+        kw["softmax_scale"] = float(rng.choice([0.0, -0.5, np.inf, np.nan]))
+    elif rule == "docs_overlap":  # document b starts inside document a
+        a, b = (int(x) for x in rng.choice(nd, 2, replace=False))
+        kw["doc_kv_offset"][b] = kw["doc_kv_offset"][a] + int(rng.integers(0, kw["doc_len"][a]))
+    return rule
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_invalid_descriptors_rejected(seed):
+    """Random pools with one rule of ca_plan_create broken at a time are
+    refused with CA_ERR_INVALID_ARG on the host (and planned when intact)."""
+    rng = np.random.default_rng(30_000 + seed)
+    w = random_pool(seed)
+    ca.dry_run(**_descriptor(w))
+    for _ in range(12):
+        kw = _descriptor(w)
+        rule = _break_one_rule(kw, rng)
+        with pytest.raises(ca.CAError) as ei:
+            ca.dry_run(**kw)
+        assert ei.value.status == capi.CA_ERR_INVALID_ARG, (rule, str(ei.value))
+
+
 def test_merge_rejects_sizes_that_overflow_the_launch():
     """ca_merge validates its sizes on the host before any CUDA call."""
     with pytest.raises(ca.CAError) as ei:

@@ -1,7 +1,8 @@
 """GPU parity on seeded random CA-task pools against the fp64 oracle: forward
 (float32 O element by element, LSE, bf16 O = RNE of float32 O), backward
-(dQ, dK, dV) and, where it applies, the CTA-pair backward (dK, dV bit for bit
-with the one-CTA kernel).  The pools mix what the fixed cases test one at a
+(dQ, dK, dV), the forward with its items cut into parts of 1 and 2 key tiles
+(in-launch split-KV and merge) and, where it applies, the CTA-pair backward
+(dK, dV bit for bit with the one-CTA kernel).  The pools mix what the fixed cases test one at a
 time: G from 1 to 128, head_dim 64 and 128, shards in random order, rows no
 task asks for, KV blocks starting past 0 or ending before a shard's rows,
 gaps between documents in K/V, and random (sink, lo, window) masks."""
@@ -13,7 +14,7 @@ import document_masked_core_gb300 as ca
 import oracle
 import workloads as W
 from cases import random_pool
-from parity import check_grad, check_lse, check_o, rel_fro, to64
+from parity import O_ATOL, check_grad, check_lse, check_o, rel_fro, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -95,3 +96,29 @@ def test_random_pool_matches_oracle(w):
         s, p = out[kinds[0]], out[kinds[1]]
         assert torch.equal(s[1], p[1]) and torch.equal(s[2], p[2])
         assert rel_fro(to64(p[0]), to64(s[0])) <= 1e-4
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("split", [1, 2])
+def test_random_pool_split_forward_matches_oracle(w, split):
+    """Every item cut into parts of `split` key tiles, merged in the launch."""
+    q, k, v, _ = W.make_tensors(w, device="cuda", need_grad_inputs=False)
+    torch.cuda.synchronize()
+    O, LSE = oracle.forward(oracle.Problem(w, q.cpu(), k.cpu(), v.cpu()))
+    res = {}
+    for kv_split in (split, -1):
+        plan = ca.Plan.from_workload(w, o_dtype=ca.CA_DTYPE_FP32)
+        plan.set_kv_split(kv_split)
+        ws = ca.workspace(plan)
+        o, lse = ca.alloc_forward(plan)
+        o.fill_(float("nan"))
+        plan.forward(q, k, v, o, lse, ws)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        res[kv_split] = (plan.info(), o, lse)
+    info_s, o_s, l_s = res[split]
+    info_n, o_n, l_n = res[-1]
+    assert info_s["fwd_tile_pairs"] == info_n["fwd_tile_pairs"]
+    check_o(to64(o_s), O, "O (split)")
+    check_lse(to64(l_s), LSE, "LSE (split)")
+    assert (o_s - o_n).abs().max().item() <= O_ATOL
