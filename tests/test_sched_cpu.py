@@ -228,6 +228,26 @@ def test_library_schedule_equals_oracle(name, k):
         assert res["max_load"] == st["max_load"] and res["min_load"] == st["min_load"]
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_library_schedule_equals_oracle_on_random_documents(seed):
+    """Random document sets (1-40 documents of log-uniform length up to 200K
+    tokens), server counts, tolerances, shard floors and byte costs: the
+    library's schedule equals the oracle's task by task, with the same counts
+    and the same bytes moved."""
+    rng = np.random.default_rng(40_000 + seed)
+    docs = [int(x) for x in np.exp(rng.uniform(0, np.log(200_000), int(rng.integers(1, 41)))).astype(np.int64) + 1]
+    k = int(rng.integers(1, 17))
+    bq, bkv = float(rng.uniform(256, 16384)), float(rng.uniform(128, 8192))
+    eps = float(rng.choice([0.0, 0.01, 0.05]))
+    min_shard = int(rng.choice([0, 32, 128, 1024]))
+    got, res = capi.schedule(docs, k, bq, bkv, tolerance=eps, min_shard_tokens=min_shard)
+    exp, st = O.schedule(docs, k, bq, bkv, tolerance=eps, min_shard_tokens=min_shard)
+    assert as_tuples(got) == [tuple(t) for t in exp]
+    assert res["n_migrations"] == st["n_migrations"] and res["n_splits"] == st["n_splits"]
+    assert res["comm_bytes"] == st["comm_bytes"]
+    assert res["max_load"] == st["max_load"] and res["min_load"] == st["min_load"]
+
+
 def test_library_rejects_bad_arguments():
     with pytest.raises(capi.CAError):
         capi.schedule([], 2, 1.0, 1.0)
