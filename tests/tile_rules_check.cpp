@@ -2,6 +2,7 @@
 // (document_masked_core_gb300/csrc/ca_internal.h) against brute-force
 // enumeration of the visibility rule of include/ca.h (ca_task_t and
 // ca_mask_t), on random tasks:
+//   rows:     row_keys' two key intervals hold exactly the keys a row sees;
 //   forward:  for every pair of query tiles (an item), key_tile_ranges gives
 //             an increasing sequence of key tiles and visits_upto a prefix of
 //             it for each tile; the prefix holds every key tile a row of the
@@ -59,11 +60,18 @@ int main(int argc, char **argv) {
         const int tpt = 1 << uni(0, 7);
         const int32_t q_end = t.q_start + t.q_len;  // one past the last row
         const int32_t n_keytiles = (L + 127) / 128;
-        // brute force: bit jt of seen[p] is set when row p sees some key of key tile jt
+        // brute force: bit jt of seen[p] is set when row p sees some key of key tile jt;
+        // row_keys' two intervals [a, r1) U [r2, hi) hold exactly the keys row p sees
         std::vector<uint32_t> seen(L, 0);
-        for (int32_t p = 0; p < L; ++p)
-            for (int32_t j = 0; j <= p; ++j)
-                if (visible(t, p, j)) seen[p] |= 1u << (j / 128);
+        for (int32_t p = 0; p < L; ++p) {
+            const ca::RowKeys k = ca::row_keys(t, p);
+            for (int32_t j = 0; j < L; ++j) {
+                const bool vis = visible(t, p, j);
+                if (vis != (j >= k.a && (j < k.r1 || (j >= k.r2 && j < k.hi))))
+                    return fail(t, 1, "row_keys intervals", p, j);
+                if (vis) seen[p] |= 1u << (j / 128);
+            }
+        }
         auto furthest = [&](int32_t p0, int32_t p1) {  // furthest key tile rows [p0, p1] see, -1: none
             int32_t f = -1;
             for (int32_t p = p0; p <= p1; ++p)
